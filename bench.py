@@ -1,0 +1,392 @@
+"""Benchmark of the weight-only quantized GEMV hot path on GB300.
+
+One step = one decode step through L layers, each layer running the three
+batch-1 GEMVs of the headline metric on its own weights:
+  W8: int8, group-128 fp32 scales, K = N = 4096, fp32 x / y
+  W3: 3-bit, per-column fp16 scale and zero, K = N = 4096, fp16 x / y
+  W4: 4-bit act-order (g_idx), group-128 fp16 scales and 4-bit zeros,
+      K = 4096, N = 11008, fp16 x / y
+The L layers' weights are distinct (L * 47 MB > 3x the L2 cache), so every
+GEMV streams its weights from HBM.  The kernels of a step are captured in one
+CUDA graph and chained with programmatic dependent launch.
+
+value = algorithmic bytes (packed weights + scales + zeros + g_idx + x + y)
+of all GEMVs of all steps / device time of the timed steps, in GB/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% of roofline), W3/W4/W8 GEMV K=N=4096, M=1"
+LAYERS = 16
+WORKLOAD = ("decode step through 16 layers, each: W8 g128 GEMV 4096x4096 (fp32) + W3 per-column GEMV "
+            "4096x4096 (fp16) + W4 act-order g128 GEMV 4096x11008 (fp16), M=1")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def alg_bytes_w8(M=1, K=4096, N=4096, g=128):
+    return K * N + (K // g) * N * 4 + M * K * 4 + M * N * 4
+
+
+def alg_bytes_w3(M=1, K=4096, N=4096):
+    return (3 * K // 32) * N * 4 + N * 2 * 2 + M * K * 2 + M * N * 2
+
+
+def alg_bytes_w4g(M=1, K=4096, N=11008, g=128):
+    G = K // g
+    return (K // 8) * N * 4 + G * N * 2 + G * (N // 8) * 4 + K * 4 + M * K * 2 + M * N * 2
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ inputs ----
+
+def make_layer_inputs(layer: int):
+    """Seeded inputs of one layer (numpy).  Layer l uses seeds 1000*l + {1, 2, 3}."""
+    import synthetic as syn
+    base = 1000 * layer
+    return (syn.make_wq8(seed=base + 1), syn.make_wq3(seed=base + 2), syn.make_wq4_actorder(seed=base + 3))
+
+
+def to_dev(a, dev):
+    import numpy as np
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+class Layer:
+    def __init__(self, d8, d3, d4, dev):
+        import torch
+        self.w8 = {k: to_dev(d8[k], dev) for k in ("x", "w", "scales")}
+        self.w3 = {k: to_dev(d3[k], dev) for k in ("x", "mat", "scales", "zeros")}
+        self.w4 = {k: to_dev(d4[k], dev) for k in ("x", "qweight", "scales", "qzeros", "g_idx")}
+        self.y8 = torch.empty((1, 4096), dtype=torch.float32, device=dev)
+        self.y3 = torch.empty((1, 4096), dtype=torch.float16, device=dev)
+        self.y4 = torch.empty((1, 11008), dtype=torch.float16, device=dev)
+
+    def run_w8(self, wq, flags, stream):
+        t = self.w8
+        wq.wq8_gemv(t["x"], t["w"], t["scales"], self.y8, 1, 4096, 4096, 128, flags=flags, stream=stream)
+
+    def run_w3(self, wq, flags, stream):
+        t = self.w3
+        wq.wq3_gemv(t["x"], t["mat"], t["scales"], t["zeros"], self.y3, 1, 4096, 4096, flags=flags, stream=stream)
+
+    def run_w4(self, wq, flags, stream):
+        t = self.w4
+        wq.wq4_gemm(t["x"], t["qweight"], t["scales"], t["qzeros"], t["g_idx"], self.y4, 1, 4096, 11008, 128,
+                    wq.WQ_F16, flags=flags, stream=stream)
+
+
+# -------------------------------------------------------------- our arm ----
+
+def run_ours(args, rank, world, dev):
+    import numpy as np
+    import torch
+
+    import gemm_dequant_gemv_gb300 as wq
+
+    torch.cuda.set_device(dev)
+    layers = [Layer(*make_layer_inputs(l + LAYERS * rank), dev) for l in range(LAYERS)]
+    step_bytes = LAYERS * (alg_bytes_w8() + alg_bytes_w3() + alg_bytes_w4g())
+    stream = torch.cuda.Stream(device=dev)
+    s = stream.cuda_stream
+    PDL = wq.WQ_FLAG_PDL
+
+    # one step as a CUDA graph: per layer W4 (timed with an event pair), W8, W3
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
+
+    def step(record_events):
+        for i, L in enumerate(layers):
+            if record_events:
+                ev[i][0].record(stream)
+            L.run_w4(wq, PDL, s)
+            if record_events:
+                ev[i][1].record(stream)
+            L.run_w8(wq, PDL, s)
+            L.run_w3(wq, PDL, s)
+
+    with torch.cuda.stream(stream):
+        step(False)  # eager warm-up of every kernel instance before capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(True)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
+    gpu_id = torch.cuda.get_device_properties(dev).uuid
+    gpu_id = f"GPU-{gpu_id}" if gpu_id and not str(gpu_id).startswith("GPU-") else str(gpu_id)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    w4_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(LAYERS)]
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API, host buffers: x in (pinned), y out (pinned), per step
+    e2e_steps = max(3, min(args.steps, 50))
+    hx = [(torch.empty_like(L.w8["x"], device="cpu").pin_memory(), torch.empty_like(L.w3["x"], device="cpu").pin_memory(),
+           torch.empty_like(L.w4["x"], device="cpu").pin_memory()) for L in layers]
+    hy = [(torch.empty_like(L.y8, device="cpu").pin_memory(), torch.empty_like(L.y3, device="cpu").pin_memory(),
+           torch.empty_like(L.y4, device="cpu").pin_memory()) for L in layers]
+    for i, L in enumerate(layers):
+        hx[i][0].copy_(L.w8["x"]); hx[i][1].copy_(L.w3["x"]); hx[i][2].copy_(L.w4["x"])
+    h2d = sum(int(t.numel() * t.element_size()) for tri in hx for t in tri)
+    d2h = sum(int(t.numel() * t.element_size()) for tri in hy for t in tri)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for i, L in enumerate(layers):
+                L.w8["x"].copy_(hx[i][0], non_blocking=True)
+                L.w3["x"].copy_(hx[i][1], non_blocking=True)
+                L.w4["x"].copy_(hx[i][2], non_blocking=True)
+                L.run_w4(wq, PDL, s)
+                L.run_w8(wq, PDL, s)
+                L.run_w3(wq, PDL, s)
+                hy[i][0].copy_(L.y8, non_blocking=True)
+                hy[i][1].copy_(L.y3, non_blocking=True)
+                hy[i][2].copy_(L.y4, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    te = time.perf_counter() - te
+    if world > 1:
+        t = torch.tensor([te], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        te = float(t.item())
+
+    return dict(ms=ms, w4_us=w4_us, clocks=clk.summary(), step_bytes=step_bytes,
+                e2e_s_per_step=te / e2e_steps, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps)
+
+
+# ------------------------------------------------------------- the oracle ----
+
+def oracle_step(d8, d3, d4, cols8=None, cols3=None, cols4=None):
+    import numpy as np
+
+    import oracle
+    oracle.wq8_gemv(d8["x"], d8["w"], d8["scales"], 128, cols=cols8)
+    oracle.wq3_gemv(d3["x"].view(np.uint16), d3["mat"], d3["scales"].view(np.uint16), d3["zeros"].view(np.uint16),
+                    cols=cols3)
+    oracle.wq4_gemm(d4["x"].view(np.uint16), 0, d4["qweight"], d4["scales"].view(np.uint16), d4["qzeros"],
+                    d4["g_idx"], 128, cols=cols4)
+
+
+def sample_bytes(n8, n3, n4):
+    """Algorithmic bytes of the oracle sample restricted to n8/n3/n4 output columns."""
+    return (alg_bytes_w8() * n8 / 4096 + alg_bytes_w3() * n3 / 4096 + alg_bytes_w4g() * n4 / 11008)
+
+
+def cpu_baseline(budget_s=10.0):
+    """The oracle as it stands, single-threaded, on whole steps of one layer."""
+    import oracle
+    oracle.build()
+    d8, d3, d4 = make_layer_inputs(0)
+    t = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(d8, d3, d4)
+        n += 1
+        if time.perf_counter() - t >= budget_s:
+            break
+    dt = time.perf_counter() - t
+    b = n * sample_bytes(4096, 4096, 11008)
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full single-layer steps (W8 + W3 + W4 act-order GEMVs, every output column), "
+                      f"{dt:.1f} s single-threaded C oracle"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step a column sample of one layer's GEMVs,
+    sized so that the whole run takes about a minute."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    d8, d3, d4 = make_layer_inputs(0)
+    r = np.random.default_rng(0)
+    probe = r.choice(4096, 64, replace=False)
+    t = time.perf_counter()
+    oracle_step(d8, d3, d4, probe, probe, probe)
+    per_col = (time.perf_counter() - t) / 64
+    total_steps = max(1, args.steps + args.warmup)
+    ncols = int(max(1, min(4096, 60.0 / (total_steps * max(per_col, 1e-9)))))
+    c8, c3 = r.choice(4096, ncols, replace=False), r.choice(4096, ncols, replace=False)
+    c4 = r.choice(11008, ncols, replace=False)
+    for _ in range(args.warmup):
+        oracle_step(d8, d3, d4, c8, c3, c4)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(d8, d3, d4, c8, c3, c4)
+    dt = time.perf_counter() - t
+    b = args.steps * sample_bytes(ncols, ncols, ncols)
+    value = b / dt / 1e9
+    sample = (f"each step: {ncols} sampled output columns of each of the three GEMVs of one layer "
+              f"(single-threaded C oracle)")
+    return {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": 1, "M": 1, "sample_columns": ncols},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# -------------------------------------------------------------------- main ----
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    dev = torch.device(f"cuda:{local}")
+    if world > 1:
+        torch.cuda.set_device(dev)
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = run_ours(args, rank, world, dev)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peaks()
+    total_bytes = res["step_bytes"] * args.steps * world
+    value = total_bytes / (res["ms"] * 1e-3) / 1e9
+    w4_us = statistics.mean(res["w4_us"])
+    achieved = alg_bytes_w4g() / (w4_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": LAYERS, "M": 1,
+                   "l2": f"inputs larger than L2: {LAYERS} distinct weight sets, "
+                         f"{res['step_bytes'] / 1e6:.0f} MB per step",
+                   "us_per_call_mean": res["ms"] / args.steps * 1e3 / (3 * LAYERS),
+                   "w4_actorder_us_per_launch": w4_us},
+        "roofline": {"bound": "hbm", "kernel": "k4g_gemv_kernel (W4 act-order GEMV 4096x11008)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind, "traffic": None},
+        "e2e": {"value": res["step_bytes"] / res["e2e_s_per_step"] / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "steps": res["e2e_steps"]},
+        "gpu_launches": 3 * LAYERS * args.steps,
+        "clocks": res["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

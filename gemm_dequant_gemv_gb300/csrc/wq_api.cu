@@ -1,0 +1,250 @@
+// wq_api.cu -- the C ABI of libwq.so: argument validation, tensor-map
+// encoding, launch planning and dispatch to the kernels.  See include/wq.h for
+// the contract of every entry point.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/wq.h"
+#include "wq_gemv_common.cuh"
+#include "wq_launch.h"
+#include "wq_mma.h"
+
+namespace wq {
+
+__device__ unsigned int g_timeout_flag = 0;
+
+namespace {
+
+constexpr int kMaxDim = 1 << 24;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that the
+// library has no link-time dependency on libcuda.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// 2D row-major tensor [outer, inner] of `dt` elements, box [box_outer, box_inner],
+// no swizzle, out-of-bounds elements read as zero.
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int device_max_smem() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes, const CUtensorMap& map,
+                               const GemvArgs& a) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.S, p.T, 1);
+  cfg.blockDim = dim3(kGemvThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (p.S > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = p.S;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (p.flags & WQ_FLAG_PDL) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  void* args[2] = {const_cast<CUtensorMap*>(&map), const_cast<GemvArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+namespace {
+
+// K-slices per column tile: enough CTAs to cover the GPU once, at most 8 (a
+// portable cluster) and at most one slice per work unit.
+int plan_splits(int tiles, int units) {
+  const int sms = std::max(1, device_sm_count());
+  int s = (sms + tiles / 2) / tiles;
+  s = std::max(1, std::min(s, 8));
+  return std::min(s, std::max(units, 1));
+}
+
+// Most scale groups any one of the S K-slices touches.
+int max_groups_per_slice(int units, int S, int unit_k, int group) {
+  int mx = 1;
+  for (int s = 0; s < S; ++s) {
+    const int u0 = static_cast<int>((static_cast<long long>(s) * units) / S);
+    const int u1 = static_cast<int>((static_cast<long long>(s + 1) * units) / S);
+    if (u1 > u0) mx = std::max(mx, (unit_k * u1 - 1) / group - (unit_k * u0) / group + 1);
+  }
+  return mx;
+}
+
+int round_mt(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+wq_status from_cuda(cudaError_t e) {
+  if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+WQ_API const char* wq_status_string(int status) {
+  switch (status) {
+    case WQ_OK: return "ok";
+    case WQ_ERR_NULL: return "a required pointer is NULL";
+    case WQ_ERR_SHAPE: return "a shape or group-size argument is out of range or not divisible";
+    case WQ_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case WQ_ERR_UNSUPPORTED: return "request not supported by this build";
+    case WQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case WQ_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case WQ_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    default: return "unknown status";
+  }
+}
+
+WQ_API int wq_abi_version(void) { return WQ_ABI_VERSION; }
+
+WQ_API int wq_read_timeout_flag(int clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_timeout_flag, sizeof v) != cudaSuccess) return -1;
+  if (clear && v) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_timeout_flag, &z, sizeof z) != cudaSuccess) return -1;
+  }
+  return static_cast<int>(v);
+}
+
+WQ_API wq_status wq8_gemv(const float* x, const int8_t* w, const float* scales, float* y, int M, int K, int N,
+                          int group_size, unsigned flags, void* stream) {
+  if (!x || !w || !scales || !y) return WQ_ERR_NULL;
+  if (M < 1 || M > 8 || K < 1 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 16 || group_size % 16 != 0 || K % group_size != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(y)) return WQ_ERR_ALIGN;
+
+  const int T = (N + 255) / 256, units = K / 8;
+  LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
+  GemvArgs a{x, y, scales, nullptr, nullptr, M, K, N, group_size, 0};
+  a.ng_max = max_groups_per_slice(units, p.S, 8, group_size);
+  if (wq8_gemv_smem_bytes(p.MT, a.ng_max) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WQ_ERR_CUDA;
+  return from_cuda(launch_wq8_gemv(p, map, a));
+}
+
+WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales, const void* zeros, void* y, int M,
+                          int K, int N, unsigned flags, void* stream) {
+  if (!x || !mat || !scales || !zeros || !y) return WQ_ERR_NULL;
+  if (M < 1 || M > 8 || K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(mat) || !aligned16(scales) || !aligned16(zeros) || !aligned16(y))
+    return WQ_ERR_ALIGN;
+
+  const int T = (N + 127) / 128, units = K / 32;
+  LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
+  GemvArgs a{x, y, scales, zeros, nullptr, M, K, N, 0, 0};
+  if (wq3_gemv_smem_bytes(p.MT) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat, N, 3 * (K / 32), size_t(N) * 4, 128, 24,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WQ_ERR_CUDA;
+  return from_cuda(launch_wq3_gemv(p, map, a));
+}
+
+WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                          const int32_t* g_idx, void* y, int M, int K, int N, int group_size, int act_dtype,
+                          void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!x || !qweight || !scales || !y) return WQ_ERR_NULL;
+  if (M < 1 || K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 32 || group_size % 32 != 0 || K % group_size != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (act_dtype != WQ_F16 && act_dtype != WQ_BF16) return WQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) ||
+      (qzeros && !aligned16(qzeros)) || (g_idx && !aligned16(g_idx)))
+    return WQ_ERR_ALIGN;
+  const int act_bf16 = act_dtype == WQ_BF16;
+
+  if (M >= 16 && !g_idx) {
+    return from_cuda(launch_wq4_mma(x, qweight, scales, qzeros, y, M, K, N, group_size, act_bf16, flags,
+                                    static_cast<cudaStream_t>(stream)));
+  }
+  if (M > 8) return WQ_ERR_UNSUPPORTED;
+
+  const int T = (N + 127) / 128, units = K / 32;
+  LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
+  GemvArgs a{x, y, scales, qzeros, g_idx, M, K, N, group_size, 0};
+  const bool act_order = g_idx != nullptr;
+  a.ng_max = act_order ? 1 : max_groups_per_slice(units, p.S, 32, group_size);
+  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, act_order, K / group_size) > static_cast<size_t>(device_max_smem()))
+    return WQ_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, 128, 32,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WQ_ERR_CUDA;
+  return from_cuda(launch_wq4_gemv(p, map, a, act_bf16, qzeros != nullptr, act_order));
+}
+
+WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N) { return w8a8_workspace_bytes(M, K, N); }
+
+WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
+                           int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace,
+                           size_t workspace_bytes, unsigned flags, void* stream) {
+  if (!X || !W || !Sw || !Y || !workspace) return (!workspace && X && W && Sw && Y) ? WQ_ERR_WORKSPACE : WQ_ERR_NULL;
+  if (M < 1 || K < 64 || N < 16 || M > kMaxDim || K > 65536 || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 64 != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Sw) || !aligned16(Y) || (Xq_out && !aligned16(Xq_out)) ||
+      (Sx_out && !aligned16(Sx_out)) || (acc_out && !aligned16(acc_out)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return WQ_ERR_ALIGN;
+  if (workspace_bytes < w8a8_workspace_bytes(M, K, N)) return WQ_ERR_WORKSPACE;
+  return from_cuda(launch_w8a8(X, W, Sw, Y, M, K, N, Xq_out, Sx_out, acc_out, workspace, flags,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

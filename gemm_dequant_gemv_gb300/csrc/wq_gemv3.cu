@@ -1,0 +1,239 @@
+// wq_gemv3.cu -- 3-bit GEMV with per-column fp16 scale and stored zero.
+//
+// Definition (GPTQ CUDA kernel walkthrough, CUDA核函數設計與實現):
+//   y[m,n] = sum_k x[m,k] * (s[n] * q(k,n) - zero[n]),  zero[n] = s[n] * z[n] stored.
+// Storage: int32 [3K/32, N]; the 32 codes of k = 32b..32b+31 of a column form
+// a 96-bit little-endian bit stream over word rows 3b..3b+2, code j at bits
+// [3j, 3j+3).
+//
+// Exact code conversion without extracting each code to bit 0: a word is
+// shifted (or funnel-shifted across two words) so that four codes sit at bit
+// offsets o in {11, 14, 17, 20}; AND with (7 << o) and OR with 0x3F000000 then
+// gives the fp32 value m = 0.5 + q 2^(o-24) exactly.  The activation is staged
+// pre-multiplied by 2^(24-o) (exact), so x' m = x 2^(23-o) + x q with an exact
+// product; the per-CTA constant B = sum_k x_k 2^(23-o(k)) is removed once:
+//   y = s (sum_k x' m - B) - zero * sum_k x.
+#include "wq_gemv_common.cuh"
+#include "wq_launch.h"
+
+namespace wq {
+namespace {
+
+constexpr int kBN = 128;
+constexpr int kUnitRows = 3;                       // one 32-code block
+constexpr int kStageRows = kConsumerWarps * kUnitRows;
+constexpr int kStageBytes = kStageRows * kBN * 4;  // 12 KB
+constexpr int kNS = 5;
+
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+
+struct Smem3 {
+  size_t xs, red2, part, bars, flag, total;
+  __host__ __device__ explicit Smem3(int MT) {
+    size_t o = size_t(kNS) * kStageBytes;
+    xs = o;   o = align16(o + size_t(kConsumerWarps) * MT * 32 * 8);
+    red2 = o; o = align16(o + size_t(kConsumerWarps) * MT * 2 * 4);   // per-warp (B, X) sums
+    part = o; o = align16(o + size_t(MT) * kBN * 4);
+    bars = o; o = align16(o + size_t(2 * kNS) * 8);
+    flag = o; o = align16(o + 16);
+    total = o;
+  }
+};
+
+// Which of the nine shifted words holds code j of a block, and in which of its
+// four slots (bit offset 11 + 3 * slot).  Shifts: w0<<11 (codes 0-3), w0>>1
+// (4-7), w0>>13 (8-9), funnel(w0,w1)>>19 (10-13), w1<<1 (14-17),
+// funnel(w1,w2)>>11 (18-21), w2<<9 (22-25), w2>>3 (26-29), w2>>15 (30-31).
+__host__ __device__ constexpr int code_src(int j) {
+  return j < 8 ? j / 4 : (j < 10 ? 2 : (j < 30 ? 3 + (j - 10) / 4 : 8));
+}
+__host__ __device__ constexpr int code_slot(int j) {
+  return j < 8 ? j % 4 : (j < 10 ? j - 8 : (j < 30 ? (j - 10) % 4 : j - 30));
+}
+__host__ __device__ constexpr int code_offset(int j) { return 11 + 3 * code_slot(j); }
+
+template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    k3_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Smem3 L(MT);
+  uint8_t* stages = smem;
+  float2* xs = reinterpret_cast<float2*>(smem + L.xs);
+  float* red2 = reinterpret_cast<float*>(smem + L.red2);
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kNS;
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = gridDim.x, n0 = blockIdx.y * kBN;
+  const int M = a.M, K = a.K, N = a.N;
+  int u0, u1;
+  split_range(K / 32, S, blockIdx.x, u0, u1);
+  const int n_loads = (u1 - u0 + kConsumerWarps - 1) / kConsumerWarps;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    *failed = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    int issued = 0;
+    if (lane == 0 && n_loads > 0)
+      issued = produce_stages<kNS, kStageBytes>(&wmap, stages, full, empty, n0, 3 * u0, kStageRows, n_loads,
+                                                failed);
+    pdl_wait();
+    if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
+  } else {
+    const __half* X = static_cast<const __half*>(a.x);
+    // this lane always stages code position j = lane of its warp's blocks
+    const int off = code_offset(lane);
+    const float fac = __int_as_float((127 + 24 - off) << 23);       // 2^(24 - off)
+    const float bfac = __int_as_float((127 + 23 - off) << 23);      // 2^(23 - off)
+    float bsum[MT], xsum[MT], acc[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      bsum[m] = xsum[m] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[m][c] = 0.f;
+    }
+    pdl_wait();
+
+    float xnext[MT];
+    auto load_x = [&](int u) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        xnext[m] = (u < u1 && m < M) ? __half2float(X[size_t(m) * K + 32 * u + lane]) : 0.f;
+    };
+    load_x(u0 + warp);
+    float2* myxs = xs + warp * MT * 32;
+    const uint32_t magic = 0x3F000000u;
+
+    for (int it = 0; it < n_loads; ++it) {
+      const int s = it % kNS;
+      const int u = u0 + it * kConsumerWarps + warp;
+      const bool active = u < u1;
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float xp = xnext[m] * fac;
+        myxs[m * 32 + lane] = make_float2(xp, xp);
+        bsum[m] = fmaf(xnext[m], bfac, bsum[m]);
+        xsum[m] += xnext[m];
+      }
+      __syncwarp();
+      load_x(u + kConsumerWarps);
+      if (!mbar_wait(&full[s], (it / kNS) & 1)) {
+        *failed = 1;
+        break;
+      }
+      if (active) {
+        const uint8_t* rowp = stages + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
+        const uint4 A = *reinterpret_cast<const uint4*>(rowp);
+        const uint4 B = *reinterpret_cast<const uint4*>(rowp + kBN * 4);
+        const uint4 C = *reinterpret_cast<const uint4*>(rowp + 2 * kBN * 4);
+        const uint32_t w0[4] = {A.x, A.y, A.z, A.w};
+        const uint32_t w1[4] = {B.x, B.y, B.z, B.w};
+        const uint32_t w2[4] = {C.x, C.y, C.z, C.w};
+        // the nine shifted words of each column: codes 0-3, 4-7, 8-9, 10-13, 14-17, 18-21, 22-25, 26-29, 30-31
+        uint32_t t[4][9];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          t[c][0] = w0[c] << 11;
+          t[c][1] = w0[c] >> 1;
+          t[c][2] = w0[c] >> 13;
+          t[c][3] = shf_r(w0[c], w1[c], 19);
+          t[c][4] = w1[c] << 1;
+          t[c][5] = shf_r(w1[c], w2[c], 11);
+          t[c][6] = w2[c] << 9;
+          t[c][7] = w2[c] >> 3;
+          t[c][8] = w2[c] >> 15;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int src = code_src(j);
+          const uint32_t mask = 7u << code_offset(j);
+          float mf[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mf[c] = as_f32((t[c][src] & mask) | magic);
+          const float2 m01 = make_float2(mf[0], mf[1]), m23 = make_float2(mf[2], mf[3]);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float2 xp = myxs[m * 32 + j];
+            float2 a01 = make_float2(acc[m][0], acc[m][1]), a23 = make_float2(acc[m][2], acc[m][3]);
+            a01 = ffma2(xp, m01, a01);
+            a23 = ffma2(xp, m23, a23);
+            acc[m][0] = a01.x; acc[m][1] = a01.y; acc[m][2] = a23.x; acc[m][3] = a23.y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // per-warp constants B and X (lane order is fixed, so the sums are deterministic)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float b = warp_sum(bsum[m]), x = warp_sum(xsum[m]);
+      if (lane == 0) {
+        red2[(warp * MT + m) * 2 + 0] = b;
+        red2[(warp * MT + m) * 2 + 1] = x;
+      }
+    }
+    consumer_sync(kConsumerThreads);
+    float* red = reinterpret_cast<float*>(stages);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
+          make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    consumer_sync(kConsumerThreads);
+    const __half* SC = static_cast<const __half*>(a.scales);
+    const __half* ZR = static_cast<const __half*>(a.zeros);
+    for (int e = threadIdx.x; e < MT * kBN; e += kConsumerThreads) {
+      const int m = e / kBN, col = e % kBN, n = n0 + col;
+      float v = 0.f, Bm = 0.f, Xm = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        v += red[(w * MT + m) * kBN + col];
+        Bm += red2[(w * MT + m) * 2 + 0];
+        Xm += red2[(w * MT + m) * 2 + 1];
+      }
+      float r = 0.f;
+      if (n < N) {
+        const float sc = __half2float(SC[n]), zr = __half2float(ZR[n]);
+        r = fmaf(sc, v - Bm, -zr * Xm);
+      }
+      part[e] = r;
+    }
+  }
+
+  __half* Y = static_cast<__half*>(a.y);
+  finish_tile<MT, kBN>(part, S, [&](int m, int col, float v) {
+    const int n = n0 + col;
+    if (m < M && n < N) Y[size_t(m) * N + n] = __float2half_rn(v);
+  });
+}
+
+}  // namespace
+
+size_t wq3_gemv_smem_bytes(int MT) { return Smem3(MT).total; }
+
+cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a) {
+  const void* kern = nullptr;
+  switch (p.MT) {
+    case 1: kern = reinterpret_cast<const void*>(k3_gemv_kernel<1>); break;
+    case 2: kern = reinterpret_cast<const void*>(k3_gemv_kernel<2>); break;
+    case 4: kern = reinterpret_cast<const void*>(k3_gemv_kernel<4>); break;
+    case 8: kern = reinterpret_cast<const void*>(k3_gemv_kernel<8>); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return launch_gemv_kernel(kern, p, Smem3(p.MT).total, map, a);
+}
+
+}  // namespace wq

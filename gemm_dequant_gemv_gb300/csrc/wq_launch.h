@@ -1,0 +1,37 @@
+// wq_launch.h -- host-side interface between the C ABI (wq_api.cu) and the
+// kernel files.  Internal to libwq.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wq {
+
+struct GemvArgs;
+
+// How a GEMV-family kernel is launched: T column tiles (grid.y) x S K-slices
+// (grid.x, one thread-block cluster of S CTAs per tile), MT = rows of x the
+// kernel instance handles (1, 2, 4 or 8).
+struct LaunchPlan {
+  int T, S, MT;
+  unsigned flags;
+  cudaStream_t stream;
+};
+
+// Generic launcher: cluster dims (S,1,1) when S > 1, programmatic dependent
+// launch when flags has WQ_FLAG_PDL.  `kern` takes (CUtensorMap, GemvArgs).
+cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes, const CUtensorMap& map,
+                               const GemvArgs& a);
+
+size_t wq8_gemv_smem_bytes(int MT, int ng_max);
+size_t wq3_gemv_smem_bytes(int MT);
+size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G);
+
+cudaError_t launch_wq8_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a);
+cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a);
+cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a, int act_bf16,
+                            bool has_z, bool act_order);
+
+}  // namespace wq

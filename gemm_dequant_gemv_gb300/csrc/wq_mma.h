@@ -1,0 +1,22 @@
+// wq_mma.h -- host-side interface of the tensor-core paths (tcgen05): the
+// 4-bit weight-only GEMM for M >= 16 and the W8A8 dynamic-quantization GEMM.
+// Internal to libwq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wq {
+
+cudaError_t launch_wq4_mma(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                           void* y, int M, int K, int N, int group, int act_bf16, unsigned flags,
+                           cudaStream_t stream);
+
+size_t w8a8_workspace_bytes(int M, int K, int N);
+
+cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
+                        int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
+                        cudaStream_t stream);
+
+}  // namespace wq

@@ -1,0 +1,22 @@
+// Placeholder for the tensor-core paths until their kernels land.
+#include "wq_mma.h"
+
+namespace wq {
+
+cudaError_t launch_wq4_mma(const void*, const int32_t*, const void*, const int32_t*, void*, int, int, int, int, int,
+                           unsigned, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+
+size_t w8a8_workspace_bytes(int M, int K, int N) {
+  (void)N;
+  if (M < 1 || K < 1) return 0;
+  return 256;
+}
+
+cudaError_t launch_w8a8(const void*, const int8_t*, const float*, void*, int, int, int, int8_t*, float*, int32_t*,
+                        void*, unsigned, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+
+}  // namespace wq

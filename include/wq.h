@@ -1,0 +1,175 @@
+/*
+ * wq.h -- C ABI of libwq.so: weight-only quantized GEMV / skinny GEMM with the
+ * dequantization fused into the weight-tile load, and the W8A8 dynamic
+ * quantization GEMM with an exact int32 product and a fused rescale epilogue.
+ * Hand-written kernels for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the definitions (web pages, by title and section):
+ *   [QC] "Quantization CUDA" (tom-jerr.github.io): Dynamic Quantization,
+ *        优化 (fused rescale), Int8 Weight Only Quantization, Int4 Weight Only
+ *        Quantization / Weight Store, Weight Only Quantization / 量化粒度,
+ *        Marlin 格式.
+ *   [GK] GPTQ CUDA kernel walkthrough (yelogs.com): CUDA核函數設計與實現 and
+ *        C++封裝層實現 (vecquant3matmul(vec, mat, mul, scales, zeros)).
+ *   [FD] "融合反量化与GEMM：LLM推理的CUDA内核优化实践" (zingnex.cn):
+ *        核心优化思路 (dequantize inside the tile load, never write the
+ *        dequantized weights back) and 量化策略：分组对称INT8.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every data pointer is a DEVICE pointer of the current CUDA device,
+ *   owned by the caller; the library never allocates, frees or synchronizes.
+ *   `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls are stream-ordered and asynchronous.
+ * Layouts (row-major, no padding):
+ *   x        [M, K]  activations;
+ *   weights  K rows by N columns, N contiguous; packed formats pack
+ *            consecutive k of ONE column into a 32-bit word:
+ *              int8   : int8  [K, N];
+ *              4-bit  : int32 [K/8, N], nibble j (bits 4j..4j+3) of word [r, n]
+ *                       is the code of row 8r + j;
+ *              3-bit  : int32 [3K/32, N]; the 32 codes of rows 32b..32b+31 of a
+ *                       column form a 96-bit little-endian bit stream over word
+ *                       rows 3b, 3b+1, 3b+2; code j occupies stream bits
+ *                       [3j, 3j+3) (codes 10 and 21 straddle two words);
+ *   scales   [K/group, N] (group-wise) or [N] (per column);
+ *   qzeros   int32 [K/group, N/8], nibble j of word [g, c] = zero of column 8c+j;
+ *   y        [M, N], overwritten (never accumulated into).
+ * Alignment.  x, weights, scales, zeros, y (and W8A8 buffers) must be 16-byte
+ *   aligned; N must be a multiple of 8 (16 for int8 weights).
+ * Validation.  Every call validates all arguments before any CUDA call and
+ *   returns an error with no side effect.  Launch failures are reported as
+ *   WQ_ERR_CUDA (from cudaGetLastError right after the launch); errors that
+ *   happen while the kernel runs surface at the caller's next synchronization.
+ * Flags.  WQ_FLAG_PDL launches with programmatic dependent launch: the kernel
+ *   may start while the preceding kernel on the stream is still running and
+ *   prefetches its WEIGHTS, scales, zeros and g_idx before waiting for it; it
+ *   waits before reading x and before writing anything.  Do not set it when the
+ *   preceding kernel writes the weights.  0 = ordinary stream ordering.
+ * Threads.  The library keeps no mutable global state: calls may be issued
+ *   from several host threads and on several streams concurrently, provided
+ *   their output and workspace buffers are distinct.
+ */
+#ifndef WQ_H
+#define WQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WQ_API __attribute__((visibility("default")))
+#else
+#define WQ_API
+#endif
+
+#define WQ_ABI_VERSION 1
+
+typedef enum wq_status {
+  WQ_OK = 0,
+  WQ_ERR_NULL = 1,        /* a required pointer is NULL */
+  WQ_ERR_SHAPE = 2,       /* M, K, N or group size out of range / not divisible */
+  WQ_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  WQ_ERR_UNSUPPORTED = 4, /* valid request this build does not implement (dtype, M) */
+  WQ_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the size query */
+  WQ_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed */
+  WQ_ERR_TIMEOUT = 7      /* reserved: a bounded device-side wait gave up */
+} wq_status;
+
+typedef enum wq_dtype { WQ_F16 = 1, WQ_BF16 = 2 } wq_dtype;
+
+#define WQ_FLAG_PDL 1u
+
+/* Human-readable name of a status code (static string, never NULL). */
+WQ_API const char* wq_status_string(int status);
+
+/* WQ_ABI_VERSION of the built library. */
+WQ_API int wq_abi_version(void);
+
+/* Value of the device-wide timeout flag of the current device: 1 if a bounded
+ * device-side wait in any kernel of this library gave up since the flag was
+ * last cleared (the outputs of that launch are then not valid), 0 otherwise,
+ * -1 if the flag could not be read.  Synchronous (a device-to-host copy);
+ * clear != 0 also resets it. */
+WQ_API int wq_read_timeout_flag(int clear);
+
+/*
+ * wq8_gemv -- INT8 weight-only GEMV with group-wise fp32 scales.
+ *   y[m,n] = sum_k x[m,k] * scales[k/group, n] * w[k,n]
+ * [QC] Int8 Weight Only Quantization (Y = X.(Wint*Sw), fp32 accumulation);
+ * [FD] 量化策略：分组对称INT8 (symmetric INT8, one scale per 128 along K).
+ *   x      fp32 [M, K]      w      int8 [K, N]
+ *   scales fp32 [K/group, N] y     fp32 [M, N]
+ *   1 <= M <= 8; K >= 1, K % group == 0, group % 16 == 0; N % 16 == 0.
+ */
+WQ_API wq_status wq8_gemv(const float* x, const int8_t* w, const float* scales, float* y,
+                          int M, int K, int N, int group_size, unsigned flags, void* stream);
+
+/*
+ * wq3_gemv -- 3-bit GEMV with per-column fp16 scale and stored fp16 zero.
+ *   y[m,n] = sum_k x[m,k] * (scales[n] * q(k,n) - zeros[n])
+ * where zeros[n] already holds scale * zero point.
+ * [GK] CUDA核函數設計與實現 (res += (scale * q - zero) * vec[k]) and
+ *      C++封裝層實現 (vecquant3matmul(vec, mat, mul, scales, zeros)).
+ *   x      fp16 [M, K]      mat    int32 [3K/32, N]
+ *   scales fp16 [N]         zeros  fp16 [N]        y  fp16 [M, N]
+ *   1 <= M <= 8; K % 32 == 0; N % 8 == 0.  Accumulation is fp32.
+ */
+WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
+                          const void* zeros, void* y, int M, int K, int N,
+                          unsigned flags, void* stream);
+
+/*
+ * wq4_gemm -- 4-bit group-wise weight-only GEMV / skinny GEMM.
+ *   y[m,n] = sum_k x[m,k] * scales[g(k), n] * (q(k,n) - z(g(k), n))
+ *   g(k) = g_idx[k] if g_idx != NULL (act-order), else k / group;
+ *   z = the nibble of qzeros if qzeros != NULL, else 8 (symmetric).
+ * [QC] 量化粒度 (x = S*(q - Z), group-wise), Marlin 格式 (eight INT4 per
+ *      INT32, W = (Wint4 - Zero) * Scale), Int4 Weight Only Quantization.
+ *   x      act_dtype [M, K]             qweight int32 [K/8, N]
+ *   scales act_dtype [K/group, N]       qzeros  int32 [K/group, N/8] or NULL
+ *   g_idx  int32 [K] with values in [0, K/group), or NULL
+ *   y      act_dtype [M, N]
+ *   act_dtype: WQ_F16 or WQ_BF16.  M >= 1; K % group == 0, group % 32 == 0;
+ *   N % 8 == 0.  M <= 8 runs on CUDA cores; M >= 16 (no g_idx) on tcgen05
+ *   tensor cores; other M return WQ_ERR_UNSUPPORTED in this build.
+ *   workspace: none is needed; pass NULL and 0.
+ */
+WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* scales,
+                          const int32_t* qzeros, const int32_t* g_idx, void* y,
+                          int M, int K, int N, int group_size, int act_dtype,
+                          void* workspace, size_t workspace_bytes,
+                          unsigned flags, void* stream);
+
+/*
+ * w8a8_gemm -- W8A8 dynamic-quantization GEMM.
+ *   Sx[m]    = fp32(max_k |X[m,k]| / 127)              (fp32 division)
+ *   Xq[m,k]  = clamp(rint(fp32(X[m,k] / Sx[m])), -127, 127)   (ties to even;
+ *              an all-zero row has Sx = 0 and Xq = 0)
+ *   acc[m,n] = sum_k Xq[m,k] * W[k,n]                  (exact int32)
+ *   Y[m,n]   = bf16(Sx[m] * acc[m,n] * Sw[n])          (the int32 product is
+ *              never stored unless acc_out is given)
+ * [QC] Dynamic Quantization (Y = Sx*(Xint.Wint)*Sw, int8 multiply, int32
+ *      accumulate, float rescale), 优化 (multiply fused into the matmul so the
+ *      int32 result is not materialized), 量化粒度 (per-token, per-channel).
+ *   X    bf16 [M, K]     W  int8 [K, N]     Sw  fp32 [N]     Y  bf16 [M, N]
+ *   Xq_out int8 [M, K] or NULL; Sx_out fp32 [M] or NULL;
+ *   acc_out int32 [M, N] or NULL (debug: writes the exact product);
+ *   workspace >= w8a8_gemm_workspace_bytes(M, K, N) bytes, 256-byte aligned.
+ *   M >= 1; K % 64 == 0, K <= 65536; N % 16 == 0.
+ */
+WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void* Y,
+                           int M, int K, int N, int8_t* Xq_out, float* Sx_out,
+                           int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                           unsigned flags, void* stream);
+
+/* Bytes of device workspace w8a8_gemm needs for this shape (0 on bad shape). */
+WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ_H */

@@ -1,0 +1,170 @@
+"""GPU parity of the CUDA-core GEMV kernels against the oracle.
+
+Every case compares each output element with the oracle's exact value under
+|y - y_ref| <= 1e-3 * sum_k |x_k w_kn| + 1e-5, with outputs poisoned with NaN
+beforehand (an unwritten element fails) and a canary tail after each output
+(an out-of-bounds write fails).  Shapes cover several tiles and K-slices,
+ragged column tiles, one-group K, M from 1 to 8, and the full workload sizes
+in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    import gpu_util  # imports the library: fails loudly when it is missing
+    return gpu_util
+
+
+def _tol(y, y_ref, a):
+    from tolerance import within
+    ok, worst = within(y, y_ref, a)
+    assert ok, f"max |err|/bound = {worst:.3g}"
+    return worst
+
+
+# ------------------------------------------------------------------- int8 ----
+WQ8_CASES = [(1, 128, 16, 128), (1, 512, 272, 128), (3, 1024, 512, 64), (8, 256, 48, 16),
+             (2, 2048, 1040, 128), (1, 4096, 4096, 128), (5, 4096, 4096, 128)]
+
+
+@pytest.mark.parametrize("M,K,N,g", WQ8_CASES)
+def test_wq8_parity(G, M, K, N, g):
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq8(seed=1, M=M, K=K, N=N, group=g)
+    y = G.run_wq8(d)
+    y_ref, a = oracle.wq8_gemv(d["x"], d["w"], d["scales"], g)
+    _tol(G.to_f64(y), y_ref, a)
+
+
+def test_wq8_onehot_exact(G):
+    """x = e_k returns fp32(s * q) exactly (one rounding of an exact product)."""
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq8(seed=7, M=1, K=1024, N=512, group=128)
+    for k in (0, 127, 128, 513, 1023):
+        d["x"] = np.zeros((1, 1024), np.float32)
+        d["x"][0, k] = 1.0
+        y = G.to_f64(G.run_wq8(d))
+        y_ref, _ = oracle.wq8_gemv(d["x"], d["w"], d["scales"], 128)
+        assert np.array_equal(y, y_ref.astype(np.float32).astype(np.float64)), k
+
+
+# ------------------------------------------------------------------- 3-bit ----
+WQ3_CASES = [(1, 32, 8), (1, 96, 136), (2, 1024, 1000), (8, 512, 256), (1, 4096, 4096), (3, 4096, 4096)]
+
+
+@pytest.mark.parametrize("M,K,N", WQ3_CASES)
+def test_wq3_parity(G, M, K, N):
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq3(seed=2, M=M, K=K, N=N)
+    y = G.run_wq3(d)
+    y_ref, a = oracle.wq3_gemv(d["x"].view(np.uint16), d["mat"], d["scales"].view(np.uint16),
+                               d["zeros"].view(np.uint16))
+    _tol(G.to_f64(y), y_ref, a)
+
+
+def test_wq3_onehot_exact(G):
+    """Every code position of a block, including the straddling codes 10 and 21."""
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq3(seed=5, M=1, K=256, N=136)
+    for k in list(range(32)) + [32 * 5 + 10, 32 * 7 + 21, 255]:
+        x = np.zeros((1, 256), np.float16)
+        x[0, k] = 1.0
+        d["x"] = x
+        y = G.bits_u16(G.run_wq3(d))
+        y_ref, _ = oracle.wq3_gemv(x.view(np.uint16), d["mat"], d["scales"].view(np.uint16),
+                                   d["zeros"].view(np.uint16))
+        assert np.array_equal(y, oracle.round_f16(y_ref)), k
+
+
+# ------------------------------------------------------------------- 4-bit ----
+WQ4_CASES = [  # M, K, N, group, bf16, asym zeros
+    (1, 256, 128, 32, False, True), (3, 512, 264, 128, True, False), (8, 1024, 520, 64, False, True),
+    (2, 2048, 1032, 128, True, True), (1, 8192, 28672, 128, True, False), (8, 8192, 28672, 128, True, False)]
+
+
+def _make_wq4(M, K, N, g, bf16, asym, seed=4):
+    import synthetic as syn
+    if bf16 and not asym:
+        return syn.make_wq4_sym(seed=seed, M=M, K=K, N=N, group=g)
+    r = np.random.default_rng(seed)
+    codes = r.integers(0, 16, (K, N), dtype=np.uint8)
+    G_ = K // g
+    s = r.uniform(0.002, 0.03, (G_, N)).astype(np.float32)
+    x = syn.normal(seed, 1, (M, K), 1.0, np.float32)
+    if bf16:
+        xb, sb = syn.f32_to_bf16_bits(x), syn.f32_to_bf16_bits(s)
+    else:
+        xb, sb = x.astype(np.float16), s.astype(np.float16)
+    z = r.integers(0, 16, (G_, N), dtype=np.uint8)
+    return dict(x=xb, qweight=syn.pack4(codes), scales=sb, qzeros=syn.pack_zeros4(z) if asym else None,
+                g_idx=None, M=M, K=K, N=N, group=g, act_bf16=int(bf16))
+
+
+@pytest.mark.parametrize("M,K,N,g,bf16,asym", WQ4_CASES)
+def test_wq4_parity(G, M, K, N, g, bf16, asym):
+    d = _make_wq4(M, K, N, g, bf16, asym)
+    y = G.run_wq4(d)
+    cols = None
+    if N > 4096:  # sampled columns: both ends of every tile edge region plus a random sample
+        r = np.random.default_rng(0)
+        cols = np.unique(np.concatenate([np.arange(0, 256), np.arange(N - 256, N), r.integers(0, N, 1024)]))
+    y_ref, a = G.oracle_wq4(d, cols)
+    yv = G.to_f64(y)
+    _tol(yv if cols is None else yv[:, cols], y_ref, a)
+
+
+WQ4G_CASES = [(1, 256, 128, 32), (1, 1024, 392, 128), (4, 2048, 1024, 64), (1, 4096, 11008, 128),
+              (2, 4096, 11008, 128), (8, 4096, 1024, 128)]
+
+
+@pytest.mark.parametrize("M,K,N,g", WQ4G_CASES)
+def test_wq4_actorder_parity(G, M, K, N, g):
+    import synthetic as syn
+    d = syn.make_wq4_actorder(seed=3, M=M, K=K, N=N, group=g)
+    y = G.run_wq4(d)
+    y_ref, a = G.oracle_wq4(d)
+    _tol(G.to_f64(y), y_ref, a)
+
+
+@pytest.mark.parametrize("act_order", [False, True])
+def test_wq4_onehot_exact(G, act_order):
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq4_actorder(seed=9, M=1, K=512, N=264, group=128)
+    if not act_order:
+        d["g_idx"] = None
+    for k in (0, 7, 8, 129, 300, 511):
+        x = np.zeros((1, 512), np.float16)
+        x[0, k] = 1.0
+        d["x"] = x
+        y = G.bits_u16(G.run_wq4(d))
+        y_ref, _ = G.oracle_wq4(d)
+        assert np.array_equal(y, oracle.round_f16(y_ref)), k
+
+
+# ------------------------------------------------------------ invariants ----
+
+def test_repeat_bit_identical_and_pdl(G):
+    """Two runs, and a run with programmatic dependent launch, give identical bits."""
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    d = syn.make_wq4_actorder(seed=3, M=1, K=4096, N=11008, group=128)
+    y1 = G.bits_u16(G.run_wq4(d))
+    y2 = G.bits_u16(G.run_wq4(d))
+    y3 = G.bits_u16(G.run_wq4(d, flags=wq.WQ_FLAG_PDL))
+    assert np.array_equal(y1, y2) and np.array_equal(y1, y3)
+    d3 = syn.make_wq3(seed=2, M=1, K=4096, N=4096)
+    assert np.array_equal(G.bits_u16(G.run_wq3(d3)), G.bits_u16(G.run_wq3(d3, flags=wq.WQ_FLAG_PDL)))
+
+
+def test_no_timeouts(G):
+    import gemm_dequant_gemv_gb300 as wq
+    assert wq.read_timeout_flag(clear=True) == 0
