@@ -1,0 +1,346 @@
+// wq4_mma.cu -- 4-bit group-wise weight-only GEMM for M > 8 on the tcgen05
+// tensor cores (M up to 64 per launch; larger M runs in 64-row chunks).
+//
+// Definition ("Quantization CUDA", 量化粒度 and Marlin 格式):
+//   y[m,n] = sum_g s[g,n] * sum_{k in g} x[m,k] * (q(k,n) - z[g,n]).
+// The weight side is the MMA's M dimension (swap-AB): one CTA owns 128 output
+// columns, D[n, m] lives in tensor memory (128 lanes x Mp fp32 columns).
+//
+// Per 64-value k-stage:
+//   * warp 8 (TMA) loads the packed int32 words [8 rows x 128 columns] and the
+//     x tile [Mp rows x 64] (128-byte swizzle) into a ring of stages;
+//   * warps 0-3 (converters, one output column per thread) unpack the nibbles
+//     to the exact 16-bit integers q - z (PRMT into 128 + q / 1024 + q, then one
+//     packed subtraction) and write them as the K-major, 128-byte-swizzled A
+//     operand;
+//   * warp 9 issues four kind::f16 MMAs (K = 16 each) per stage into one of
+//     two tensor-memory accumulators, one accumulator per scale group;
+//   * warps 4-7 (epilogue) drain each finished group accumulator and apply the
+//     group's scale in fp32: y += s[g,n] * D_g[n,:].
+// Products (q - z) * x are exact; the only roundings are the fp32 sums.  The K
+// slices of a column tile form a thread-block cluster that reduces through
+// distributed shared memory, as in the CUDA-core kernels.
+#include <algorithm>
+
+#include "../../include/wq.h"
+#include "wq_gemv_common.cuh"
+#include "wq_mma.h"
+#include "wq_tcgen05.cuh"
+
+namespace wq {
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle);
+int device_sm_count();
+int device_max_smem();
+
+namespace {
+
+constexpr int kBN = 128;            // output columns per tile (MMA M)
+constexpr int kKS = 64;             // values of k per stage
+constexpr int kNS = 6;              // stages in the TMA ring
+constexpr int kNA = 2;              // dequantized A buffers
+constexpr int kWarpTMA = 8, kWarpMMA = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kPackedStageBytes = (kKS / 8) * kBN * 4;   // 4 KB
+constexpr int kABytes = kBN * kKS * 2;                    // 16 KB
+
+struct MmaArgs {
+  void* y;
+  const void* scales;
+  const int32_t* qzeros;
+  int M, K, N, group;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
+
+struct SmemMma {
+  size_t a, xs, pw, part, bars, misc, total;
+  __host__ __device__ explicit SmemMma(int MP) {
+    size_t o = 0;
+    a = o;    o += size_t(kNA) * kABytes;
+    xs = o;   o += size_t(kNS) * MP * 128;
+    pw = o;   o += size_t(kNS) * kPackedStageBytes;
+    part = o; o = align_up(o + size_t(MP) * kBN * 4, 16);
+    bars = o; o = align_up(o + size_t(2 * kNS + 2 * kNA + 4) * 8, 16);
+    misc = o; o = align_up(o + 32, 16);
+    total = o + 1024;  // slack to align the base to 1024 bytes
+  }
+};
+
+template <int ACT_BF16>
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (ACT_BF16)
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+template <int MP, int ACT_BF16, bool HAS_Z>
+__global__ void __launch_bounds__(kThreads, 1)
+    wq4_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const MmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemMma L(MP);
+  uint8_t* sA = smem + L.a;
+  uint8_t* sX = smem + L.xs;
+  uint8_t* sW = smem + L.pw;
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kNS;
+  uint64_t* a_full = empty + kNS;
+  uint64_t* a_empty = a_full + kNA;
+  uint64_t* t_full = a_empty + kNA;
+  uint64_t* t_empty = t_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + L.misc + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = gridDim.x, n0 = blockIdx.y * kBN;
+  const int M = a.M, K = a.K, N = a.N, gsz = a.group;
+  const int spg = gsz / kKS;  // stages per group
+  int g0, g1;
+  split_range(K / gsz, S, blockIdx.x, g0, g1);
+  const int ng = g1 - g0, nst = ng * spg, ks0 = g0 * spg;
+  constexpr uint32_t kTmemCols = (2 * MP < 32) ? 32 : 2 * MP;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kNA; ++s) {
+      mbar_init(&a_full[s], 4 * 32);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&t_full[s], 1);
+      mbar_init(&t_empty[s], 4 * 32);
+    }
+    *failed = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMMA) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+
+  float acc[MP];
+#pragma unroll
+  for (int m = 0; m < MP; ++m) acc[m] = 0.f;
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0 && nst > 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t stage_bytes = kPackedStageBytes + MP * 128;
+      const int pre = nst < kNS ? nst : kNS;
+      // weights of the first stages before the dependency wait, x after it
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(&full[i], stage_bytes);
+        tma_load_2d(sW + size_t(i) * kPackedStageBytes, &wmap, &full[i], n0, (ks0 + i) * (kKS / 8), pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(sX + size_t(i) * MP * 128, &xmap, &full[i], (ks0 + i) * kKS, 0, 0ull);
+      for (int i = kNS; i < nst && !*failed; ++i) {
+        const int s = i % kNS;
+        if (!mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
+          *failed = 1;
+          break;
+        }
+        mbar_expect_tx(&full[s], stage_bytes);
+        tma_load_2d(sW + size_t(s) * kPackedStageBytes, &wmap, &full[s], n0, (ks0 + i) * (kKS / 8), pol);
+        tma_load_2d(sX + size_t(s) * MP * 128, &xmap, &full[s], (ks0 + i) * kKS, 0, 0ull);
+      }
+    } else {
+      pdl_wait();
+    }
+  } else if (warp == kWarpMMA) {
+    // ----------------------------------------------------------------- MMA --
+    pdl_wait();
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(kBN, MP, ACT_BF16);
+      int last = -1;
+      for (int i = 0; i < nst; ++i) {
+        const int s = i % kNS, ab = i % kNA, gi = i / spg, tb = gi & 1;
+        if (i % spg == 0 && gi >= 2) {
+          if (!mbar_wait(&t_empty[tb], ((gi / 2) - 1) & 1)) { *failed = 1; break; }
+        }
+        if (!mbar_wait(&a_full[ab], (i / kNA) & 1) || !mbar_wait(&full[s], (i / kNS) & 1)) {
+          *failed = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sA + size_t(ab) * kABytes);
+        const uint32_t b_base = smem_u32(sX + size_t(s) * MP * 128);
+#pragma unroll
+        for (int k = 0; k < kKS / 16; ++k)
+          mma_f16(tmem + tb * MP, sw128_kmajor_desc(a_base + 32 * k), sw128_kmajor_desc(b_base + 32 * k), idesc,
+                  (i % spg != 0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+        mma_commit(&a_empty[ab]);
+        if (i % spg == spg - 1) mma_commit(&t_full[tb]);
+        last = i;
+      }
+      // the tensor memory is released only after the last MMA has completed
+      if (last >= 0) mbar_wait(&empty[last % kNS], (last / kNS) & 1);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------- converters --
+    const int col = threadIdx.x;  // 0..127
+    const int n = n0 + col;
+    const uint32_t magic = ACT_BF16 ? 0x43434343u : 0x64646464u;
+    uint32_t zbias = 0;
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % kNS, ab = i % kNA;
+      if (i % spg == 0) {
+        int z = 8;
+        if (HAS_Z && n < N) z = (a.qzeros[size_t(g0 + i / spg) * (N / 8) + n / 8] >> (4 * (n % 8))) & 15;
+        // 16-bit pair of (128 + z) in bf16 or (1024 + z) in fp16
+        const uint32_t h = ACT_BF16 ? (0x4300u | uint32_t(z)) : (0x6400u | uint32_t(z));
+        zbias = h | (h << 16);
+      }
+      if (!mbar_wait(&full[s], (i / kNS) & 1)) { *failed = 1; break; }
+      if (i >= kNA && !mbar_wait(&a_empty[ab], ((i / kNA) - 1) & 1)) { *failed = 1; break; }
+      const uint32_t* wrow = reinterpret_cast<const uint32_t*>(sW + size_t(s) * kPackedStageBytes) + col;
+      uint8_t* arow = sA + size_t(ab) * kABytes + size_t(col) * 128;
+#pragma unroll
+      for (int r = 0; r < kKS / 8; ++r) {
+        const uint32_t w = wrow[r * kBN];
+        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+        const uint32_t c0123 = prmt(lo, hi, 0x5140u), c4567 = prmt(lo, hi, 0x7362u);
+        uint4 v;
+        v.x = sub2<ACT_BF16>(prmt(c0123, magic, 0x4140u), zbias);
+        v.y = sub2<ACT_BF16>(prmt(c0123, magic, 0x4342u), zbias);
+        v.z = sub2<ACT_BF16>(prmt(c4567, magic, 0x4140u), zbias);
+        v.w = sub2<ACT_BF16>(prmt(c4567, magic, 0x4342u), zbias);
+        *reinterpret_cast<uint4*>(arow + ((r ^ (col & 7)) * 16)) = v;
+      }
+      fence_async_smem();
+      mbar_arrive(&a_full[ab]);
+    }
+    pdl_wait();
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    pdl_wait();
+    const int col = threadIdx.x - 4 * 32;  // 0..127 == tensor-memory lane
+    const int n = n0 + col;
+    const uint16_t* SC = static_cast<const uint16_t*>(a.scales);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    for (int gi = 0; gi < ng; ++gi) {
+      const int tb = gi & 1;
+      const float sc = (n < N) ? (ACT_BF16 ? bf16_bits_to_f32(SC[size_t(g0 + gi) * N + n])
+                                           : f16_bits_to_f32(SC[size_t(g0 + gi) * N + n]))
+                               : 0.f;
+      if (!mbar_wait(&t_full[tb], (gi / 2) & 1)) { *failed = 1; break; }
+      tc_fence_after();
+      float d[MP];
+#pragma unroll
+      for (int c = 0; c < MP; c += 16) tmem_ld16(lane_addr + tb * MP + c, d + c);
+      tc_fence_before();
+      mbar_arrive(&t_empty[tb]);
+#pragma unroll
+      for (int m = 0; m < MP; ++m) acc[m] = fmaf(sc, d[m], acc[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < MP; ++m) part[m * kBN + col] = acc[m];
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMMA) tmem_dealloc(tmem, kTmemCols);
+
+  uint16_t* Y = static_cast<uint16_t*>(a.y);
+  finish_tile<MP, kBN>(part, S, [&](int m, int c, float v) {
+    const int nn = n0 + c;
+    if (m < M && nn < N) Y[size_t(m) * N + nn] = f32_to_act<ACT_BF16>(v);
+  });
+}
+
+template <int MP, int ACT, bool HZ>
+cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaArgs& a, int T, int S,
+                       unsigned flags, cudaStream_t stream) {
+  const void* kern = reinterpret_cast<const void*>(wq4_mma_kernel<MP, ACT, HZ>);
+  const size_t smem = SmemMma(MP).total;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, T, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (S > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = S;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (flags & WQ_FLAG_PDL) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  void* args[3] = {const_cast<CUtensorMap*>(&wmap), const_cast<CUtensorMap*>(&xmap), const_cast<MmaArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+template <int MP>
+cudaError_t dispatch_mp(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaArgs& a, int T, int S,
+                        int act_bf16, bool has_z, unsigned flags, cudaStream_t stream) {
+  if (act_bf16) return has_z ? launch_mma<MP, 1, true>(wmap, xmap, a, T, S, flags, stream)
+                             : launch_mma<MP, 1, false>(wmap, xmap, a, T, S, flags, stream);
+  return has_z ? launch_mma<MP, 0, true>(wmap, xmap, a, T, S, flags, stream)
+               : launch_mma<MP, 0, false>(wmap, xmap, a, T, S, flags, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_wq4_mma(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                           void* y, int M, int K, int N, int group, int act_bf16, unsigned flags,
+                           cudaStream_t stream) {
+  if (group % kKS != 0) return cudaErrorNotSupported;
+  const int T = (N + kBN - 1) / kBN, units = K / group;
+  const int sms = std::max(1, device_sm_count());
+  int S = std::max(1, std::min(8, (sms + T / 2) / T));
+  S = std::min(S, units);
+  CUtensorMap wmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, kBN, kKS / 8,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  for (int m0 = 0; m0 < M; m0 += 64) {
+    const int mc = std::min(64, M - m0);
+    const int MP = mc <= 16 ? 16 : (mc <= 32 ? 32 : 64);
+    if (SmemMma(MP).total > static_cast<size_t>(device_max_smem())) return cudaErrorNotSupported;
+    CUtensorMap xmap;
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + size_t(m0) * K;
+    if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, xc, K, mc, size_t(K) * 2, kKS, MP,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    MmaArgs args{static_cast<uint16_t*>(y) + size_t(m0) * N, scales, qzeros, mc, K, N, group};
+    cudaError_t e;
+    switch (MP) {
+      case 16: e = dispatch_mp<16>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+      case 32: e = dispatch_mp<32>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+      default: e = dispatch_mp<64>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace wq

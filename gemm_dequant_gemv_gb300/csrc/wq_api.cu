@@ -68,8 +68,8 @@ int device_max_smem() {
   return n;
 }
 
-cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes, const CUtensorMap& map,
-                               const GemvArgs& a) {
+cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes,
+                               const CUtensorMap* const* maps, int nmaps, const GemvArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -93,19 +93,28 @@ cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t sme
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  void* args[2] = {const_cast<CUtensorMap*>(&map), const_cast<GemvArgs*>(&a)};
+  void* args[4];
+  for (int i = 0; i < nmaps; ++i) args[i] = const_cast<CUtensorMap*>(maps[i]);
+  args[nmaps] = const_cast<GemvArgs*>(&a);
   return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 namespace {
 
-// K-slices per column tile: enough CTAs to cover the GPU once, at most 8 (a
+// K-slices per column tile: about two CTAs per SM (two fit in shared memory,
+// so the next kernel's prologue can overlap this one's tail), at most 8 (a
 // portable cluster) and at most one slice per work unit.
 int plan_splits(int tiles, int units) {
   const int sms = std::max(1, device_sm_count());
-  int s = (sms + tiles / 2) / tiles;
+  int s = (2 * sms) / tiles;
   s = std::max(1, std::min(s, 8));
   return std::min(s, std::max(units, 1));
+}
+
+// Activation map: [rows, K] elements of `dt`, box = one stage's k by MT rows.
+bool encode_x_map(CUtensorMap* map, CUtensorMapDataType dt, const void* x, int K, int M, int esize, int stage_k,
+                  int MT) {
+  return encode_tensor_map_2d(map, dt, x, K, M, size_t(K) * esize, stage_k, MT, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Most scale groups any one of the S K-slices touches.
@@ -166,15 +175,16 @@ WQ_API wq_status wq8_gemv(const float* x, const int8_t* w, const float* scales, 
   if (group_size < 16 || group_size % 16 != 0 || K % group_size != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(y)) return WQ_ERR_ALIGN;
 
-  const int T = (N + 255) / 256, units = K / 8;
+  const int T = (N + 127) / 128, units = K / 8;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, nullptr, nullptr, M, K, N, group_size, 0};
   a.ng_max = max_groups_per_slice(units, p.S, 8, group_size);
   if (wq8_gemv_smem_bytes(p.MT, a.ng_max) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+  CUtensorMap wmap, xmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, K, M, 4, wq8_stage_k(), p.MT))
     return WQ_ERR_CUDA;
-  return from_cuda(launch_wq8_gemv(p, map, a));
+  return from_cuda(launch_wq8_gemv(p, wmap, xmap, a));
 }
 
 WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales, const void* zeros, void* y, int M,
@@ -189,11 +199,12 @@ WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, zeros, nullptr, M, K, N, 0, 0};
   if (wq3_gemv_smem_bytes(p.MT) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat, N, 3 * (K / 32), size_t(N) * 4, 128, 24,
-                            CU_TENSOR_MAP_SWIZZLE_NONE))
+  CUtensorMap wmap, xmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat, N, 3 * (K / 32), size_t(N) * 4, 128, 24,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, 2, wq3_stage_k(), p.MT))
     return WQ_ERR_CUDA;
-  return from_cuda(launch_wq3_gemv(p, map, a));
+  return from_cuda(launch_wq3_gemv(p, wmap, xmap, a));
 }
 
 WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
@@ -210,11 +221,11 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
     return WQ_ERR_ALIGN;
   const int act_bf16 = act_dtype == WQ_BF16;
 
-  if (M >= 16 && !g_idx) {
+  if (M > 8) {
+    if (g_idx) return WQ_ERR_UNSUPPORTED;
     return from_cuda(launch_wq4_mma(x, qweight, scales, qzeros, y, M, K, N, group_size, act_bf16, flags,
                                     static_cast<cudaStream_t>(stream)));
   }
-  if (M > 8) return WQ_ERR_UNSUPPORTED;
 
   const int T = (N + 127) / 128, units = K / 32;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
@@ -223,11 +234,13 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
   a.ng_max = act_order ? 1 : max_groups_per_slice(units, p.S, 32, group_size);
   if (wq4_gemv_smem_bytes(p.MT, a.ng_max, act_order, K / group_size) > static_cast<size_t>(device_max_smem()))
     return WQ_ERR_UNSUPPORTED;
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, 128, 32,
-                            CU_TENSOR_MAP_SWIZZLE_NONE))
+  CUtensorMap wmap, xmap, gmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, 128, 32,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, 2, wq4_stage_k(), p.MT) ||
+      (act_order && !encode_x_map(&gmap, CU_TENSOR_MAP_DATA_TYPE_INT32, g_idx, K, 1, 4, wq4_stage_k(), 1)))
     return WQ_ERR_CUDA;
-  return from_cuda(launch_wq4_gemv(p, map, a, act_bf16, qzeros != nullptr, act_order));
+  return from_cuda(launch_wq4_gemv(p, wmap, xmap, act_order ? &gmap : nullptr, a, act_bf16, qzeros != nullptr));
 }
 
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N) { return w8a8_workspace_bytes(M, K, N); }

@@ -22,16 +22,18 @@ namespace {
 constexpr int kBN = 128;
 constexpr int kUnitRows = 3;                       // one 32-code block
 constexpr int kStageRows = kConsumerWarps * kUnitRows;
+constexpr int kStageK = kConsumerWarps * 32;       // 256 values of k per stage
 constexpr int kStageBytes = kStageRows * kBN * 4;  // 12 KB
 constexpr int kNS = 5;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct Smem3 {
-  size_t xs, red2, part, bars, flag, total;
+  size_t xst, xc, red2, part, bars, flag, total;
   __host__ __device__ explicit Smem3(int MT) {
     size_t o = size_t(kNS) * kStageBytes;
-    xs = o;   o = align16(o + size_t(kConsumerWarps) * MT * 32 * 8);
+    xst = o;  o = align16(o + size_t(kNS) * MT * kStageK * 2);
+    xc = o;   o = align16(o + size_t(MT) * kStageK * 8);
     red2 = o; o = align16(o + size_t(kConsumerWarps) * MT * 2 * 4);   // per-warp (B, X) sums
     part = o; o = align16(o + size_t(MT) * kBN * 4);
     bars = o; o = align16(o + size_t(2 * kNS) * 8);
@@ -54,16 +56,19 @@ __host__ __device__ constexpr int code_offset(int j) { return 11 + 3 * code_slot
 
 template <int MT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
-    k3_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvArgs a) {
+    k3_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Smem3 L(MT);
-  uint8_t* stages = smem;
-  float2* xs = reinterpret_cast<float2*>(smem + L.xs);
+  uint8_t* wst = smem;
+  uint8_t* xst = smem + L.xst;
+  float2* xc = reinterpret_cast<float2*>(smem + L.xc);
   float* red2 = reinterpret_cast<float*>(smem + L.red2);
   float* part = reinterpret_cast<float*>(smem + L.part);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
-  volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);  // producer's
+  volatile int* cfailed = failed + 1;                                       // consumers'
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = gridDim.x, n0 = blockIdx.y * kBN;
@@ -71,6 +76,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   int u0, u1;
   split_range(K / 32, S, blockIdx.x, u0, u1);
   const int n_loads = (u1 - u0 + kConsumerWarps - 1) / kConsumerWarps;
+  constexpr uint32_t kXBytes = MT * kStageK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
@@ -78,6 +84,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       mbar_init(&empty[s], kConsumerWarps);
     }
     *failed = 0;
+    *cfailed = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -86,62 +93,53 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   if (warp == kConsumerWarps) {
     int issued = 0;
     if (lane == 0 && n_loads > 0)
-      issued = produce_stages<kNS, kStageBytes>(&wmap, stages, full, empty, n0, 3 * u0, kStageRows, n_loads,
-                                                failed);
+      issued = produce_stages<kNS>(&wmap, &xmap, wst, kStageBytes, xst, kXBytes, full, empty, n0, 3 * u0,
+                                   kStageRows, 32 * u0, kStageK, n_loads, failed);
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
   } else {
-    const __half* X = static_cast<const __half*>(a.x);
-    // this lane always stages code position j = lane of its warp's blocks
+    const int tid = threadIdx.x;
+    // this thread converts code position j = lane of every block it stages
     const int off = code_offset(lane);
-    const float fac = __int_as_float((127 + 24 - off) << 23);       // 2^(24 - off)
-    const float bfac = __int_as_float((127 + 23 - off) << 23);      // 2^(23 - off)
-    float bsum[MT], xsum[MT], acc[MT][4];
+    const float fac = __int_as_float((127 + 24 - off) << 23);   // 2^(24 - off)
+    const float bfac = __int_as_float((127 + 23 - off) << 23);  // 2^(23 - off)
+    float bsum[MT], xsum[MT];
+    float2 acc[MT][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       bsum[m] = xsum[m] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[m][c] = 0.f;
+      acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
     }
     pdl_wait();
-
-    float xnext[MT];
-    auto load_x = [&](int u) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-        xnext[m] = (u < u1 && m < M) ? __half2float(X[size_t(m) * K + 32 * u + lane]) : 0.f;
-    };
-    load_x(u0 + warp);
-    float2* myxs = xs + warp * MT * 32;
     const uint32_t magic = 0x3F000000u;
 
     for (int it = 0; it < n_loads; ++it) {
       const int s = it % kNS;
       const int u = u0 + it * kConsumerWarps + warp;
-      const bool active = u < u1;
-      __syncwarp();
+      if (!mbar_wait(&full[s], (it / kNS) & 1)) *cfailed = 1;
+      consumer_sync(kConsumerThreads);
+      if (*cfailed) break;
+      {
+        const __half* xr = reinterpret_cast<const __half*>(xst + size_t(s) * kXBytes);
+        const bool live = u < u1;  // k = 32u + lane belongs to this CTA's range
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const float xp = xnext[m] * fac;
-        myxs[m * 32 + lane] = make_float2(xp, xp);
-        bsum[m] = fmaf(xnext[m], bfac, bsum[m]);
-        xsum[m] += xnext[m];
+        for (int m = 0; m < MT; ++m) {
+          const float v = live ? __half2float(xr[m * kStageK + tid]) : 0.f;
+          const float xp = v * fac;
+          xc[m * kStageK + tid] = make_float2(xp, xp);
+          bsum[m] = fmaf(v, bfac, bsum[m]);
+          xsum[m] += v;
+        }
       }
-      __syncwarp();
-      load_x(u + kConsumerWarps);
-      if (!mbar_wait(&full[s], (it / kNS) & 1)) {
-        *failed = 1;
-        break;
-      }
-      if (active) {
-        const uint8_t* rowp = stages + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
+      consumer_sync(kConsumerThreads);
+      if (u < u1) {
+        const uint8_t* rowp = wst + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
         const uint4 A = *reinterpret_cast<const uint4*>(rowp);
         const uint4 B = *reinterpret_cast<const uint4*>(rowp + kBN * 4);
         const uint4 C = *reinterpret_cast<const uint4*>(rowp + 2 * kBN * 4);
         const uint32_t w0[4] = {A.x, A.y, A.z, A.w};
         const uint32_t w1[4] = {B.x, B.y, B.z, B.w};
         const uint32_t w2[4] = {C.x, C.y, C.z, C.w};
-        // the nine shifted words of each column: codes 0-3, 4-7, 8-9, 10-13, 14-17, 18-21, 22-25, 26-29, 30-31
         uint32_t t[4][9];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -155,21 +153,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           t[c][7] = w2[c] >> 3;
           t[c][8] = w2[c] >> 15;
         }
+        const float4* xw = reinterpret_cast<const float4*>(xc) + warp * 16;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int src = code_src(j);
-          const uint32_t mask = 7u << code_offset(j);
-          float mf[4];
+        for (int jp = 0; jp < 16; ++jp) {
+          float4 xq[MT];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) mf[c] = as_f32((t[c][src] & mask) | magic);
-          const float2 m01 = make_float2(mf[0], mf[1]), m23 = make_float2(mf[2], mf[3]);
+          for (int m = 0; m < MT; ++m) xq[m] = xw[m * (kStageK / 2) + jp];
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const float2 xp = myxs[m * 32 + j];
-            float2 a01 = make_float2(acc[m][0], acc[m][1]), a23 = make_float2(acc[m][2], acc[m][3]);
-            a01 = ffma2(xp, m01, a01);
-            a23 = ffma2(xp, m23, a23);
-            acc[m][0] = a01.x; acc[m][1] = a01.y; acc[m][2] = a23.x; acc[m][3] = a23.y;
+          for (int h = 0; h < 2; ++h) {
+            const int j = 2 * jp + h;
+            const uint32_t mask = 7u << code_offset(j);
+            const int src = code_src(j);
+            const float2 m01 = make_float2(as_f32((t[0][src] & mask) | magic), as_f32((t[1][src] & mask) | magic));
+            const float2 m23 = make_float2(as_f32((t[2][src] & mask) | magic), as_f32((t[3][src] & mask) | magic));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const float2 xp = h ? make_float2(xq[m].z, xq[m].w) : make_float2(xq[m].x, xq[m].y);
+              acc[m][0] = ffma2(xp, m01, acc[m][0]);
+              acc[m][1] = ffma2(xp, m23, acc[m][1]);
+            }
           }
         }
       }
@@ -187,15 +189,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       }
     }
     consumer_sync(kConsumerThreads);
-    float* red = reinterpret_cast<float*>(stages);
+    float* red = reinterpret_cast<float*>(wst);
 #pragma unroll
     for (int m = 0; m < MT; ++m)
       *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
-          make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
     consumer_sync(kConsumerThreads);
     const __half* SC = static_cast<const __half*>(a.scales);
     const __half* ZR = static_cast<const __half*>(a.zeros);
-    for (int e = threadIdx.x; e < MT * kBN; e += kConsumerThreads) {
+    for (int e = tid; e < MT * kBN; e += kConsumerThreads) {
       const int m = e / kBN, col = e % kBN, n = n0 + col;
       float v = 0.f, Bm = 0.f, Xm = 0.f;
 #pragma unroll
@@ -224,7 +226,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
 size_t wq3_gemv_smem_bytes(int MT) { return Smem3(MT).total; }
 
-cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a) {
+int wq3_stage_k() { return kStageK; }
+
+cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                            const GemvArgs& a) {
   const void* kern = nullptr;
   switch (p.MT) {
     case 1: kern = reinterpret_cast<const void*>(k3_gemv_kernel<1>); break;
@@ -233,7 +238,8 @@ cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& map, const G
     case 8: kern = reinterpret_cast<const void*>(k3_gemv_kernel<8>); break;
     default: return cudaErrorInvalidValue;
   }
-  return launch_gemv_kernel(kern, p, Smem3(p.MT).total, map, a);
+  const CUtensorMap* maps[2] = {&wmap, &xmap};
+  return launch_gemv_kernel(kern, p, Smem3(p.MT).total, maps, 2, a);
 }
 
 }  // namespace wq

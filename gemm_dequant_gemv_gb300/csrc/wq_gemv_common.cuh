@@ -4,15 +4,15 @@
 //   * the weight matrix is cut into column tiles of BN columns (grid.y) and
 //     the K dimension of each tile into S slices (grid.x).  The S CTAs of a
 //     tile form one thread-block cluster and add their partial results
-//     through distributed shared memory, so no partial sum ever goes to HBM;
-//   * warp 8 of each CTA is the producer: one lane streams the CTA's weight
-//     rows into a ring of NS shared-memory stages with 2D TMA loads (L2
-//     evict-first), gated by full/empty mbarriers;
-//   * warps 0..7 are consumers: each takes one "unit" (a fixed number of
-//     packed rows) of every stage, unpacks the codes in registers, converts
+//     through distributed shared memory, so no partial sum goes to HBM;
+//   * warp 8 of each CTA is the producer: one lane streams, per stage, a box
+//     of packed weight rows and the matching box of x (all M rows) into a ring
+//     of NS shared-memory stages with 2D TMA loads, gated by full/empty
+//     mbarriers.  Weights are requested before griddepcontrol.wait, x after;
+//   * warps 0..7 are consumers: per stage they first convert the stage's x
+//     block cooperatively (one named barrier), then each takes one "unit" (a
+//     fixed number of packed rows), unpacks the codes in registers, converts
 //     them with exact bit tricks and accumulates in fp32 with packed FFMA2.
-// Programmatic dependent launch: weights, scales and zeros are prefetched
-// before griddepcontrol.wait; x is read and y is written only after it.
 #pragma once
 
 #include "wq_device.cuh"
@@ -45,26 +45,36 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Producer loop: stream n_loads boxes of `rows_per_stage` rows starting at
-// packed row `row0` of column tile `col0` into the stage ring.
-template <int NS, int STAGE_BYTES>
-__device__ __forceinline__ int produce_stages(const CUtensorMap* map, uint8_t* stages, uint64_t* full,
-                                              uint64_t* empty, int col0, int row0, int rows_per_stage,
-                                              int n_loads, volatile int* cta_failed) {
-  prefetch_tensormap(map);
+// Producer loop.  Stage `it` holds packed weight rows [wrow0 + it*wrows, +wrows)
+// of column tile wcol0 (box of the weight map) and x columns
+// [xcol0 + it*xcols, +xcols) for all rows (box of the x map), both completing
+// on full[it % NS].  The weight boxes of the first NS stages are requested
+// before the programmatic-dependency wait; every x box after it.
+template <int NS>
+__device__ __forceinline__ int produce_stages(const CUtensorMap* wmap, const CUtensorMap* xmap, uint8_t* wst,
+                                              uint32_t wbytes, uint8_t* xst, uint32_t xbytes, uint64_t* full,
+                                              uint64_t* empty, int wcol0, int wrow0, int wrows, int xcol0,
+                                              int xcols, int n_loads, volatile int* cta_failed) {
+  prefetch_tensormap(wmap);
+  prefetch_tensormap(xmap);
   const uint64_t pol = l2_evict_first_policy();
-  int issued = 0;
-  for (int it = 0; it < n_loads; ++it) {
+  const int pre = n_loads < NS ? n_loads : NS;
+  for (int it = 0; it < pre; ++it) {
+    mbar_expect_tx(&full[it], wbytes + xbytes);
+    tma_load_2d(wst + size_t(it) * wbytes, wmap, &full[it], wcol0, wrow0 + it * wrows, pol);
+  }
+  pdl_wait();
+  for (int it = 0; it < pre; ++it) tma_load_2d(xst + size_t(it) * xbytes, xmap, &full[it], xcol0 + it * xcols, 0, 0ull);
+  int issued = pre;
+  for (int it = NS; it < n_loads; ++it) {
     const int s = it % NS;
-    if (it >= NS) {
-      if (*cta_failed || !mbar_wait(&empty[s], ((it / NS) - 1) & 1)) {
-        *cta_failed = 1;
-        break;
-      }
+    if (*cta_failed || !mbar_wait(&empty[s], ((it / NS) - 1) & 1)) {
+      *cta_failed = 1;
+      break;
     }
-    mbar_expect_tx(&full[s], STAGE_BYTES);
-    tma_load_2d(stages + static_cast<size_t>(s) * STAGE_BYTES, map, &full[s], col0, row0 + it * rows_per_stage,
-                pol);
+    mbar_expect_tx(&full[s], wbytes + xbytes);
+    tma_load_2d(wst + size_t(s) * wbytes, wmap, &full[s], wcol0, wrow0 + it * wrows, pol);
+    tma_load_2d(xst + size_t(s) * xbytes, xmap, &full[s], xcol0 + it * xcols, 0, 0ull);
     ++issued;
   }
   return issued;

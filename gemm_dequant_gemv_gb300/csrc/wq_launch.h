@@ -21,17 +21,26 @@ struct LaunchPlan {
 };
 
 // Generic launcher: cluster dims (S,1,1) when S > 1, programmatic dependent
-// launch when flags has WQ_FLAG_PDL.  `kern` takes (CUtensorMap, GemvArgs).
-cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes, const CUtensorMap& map,
-                               const GemvArgs& a);
+// launch when flags has WQ_FLAG_PDL.  `kern` takes nmaps CUtensorMaps
+// (__grid_constant__) followed by the GemvArgs.
+cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes,
+                               const CUtensorMap* const* maps, int nmaps, const GemvArgs& a);
 
 size_t wq8_gemv_smem_bytes(int MT, int ng_max);
 size_t wq3_gemv_smem_bytes(int MT);
 size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G);
 
-cudaError_t launch_wq8_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a);
-cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a);
-cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& map, const GemvArgs& a, int act_bf16,
-                            bool has_z, bool act_order);
+// Values of k one pipeline stage covers (the x box width of each kernel).
+int wq8_stage_k();
+int wq3_stage_k();
+int wq4_stage_k();
+
+cudaError_t launch_wq8_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                            const GemvArgs& a);
+cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                            const GemvArgs& a);
+// gmap != nullptr selects the act-order kernel (g_idx staged per stage).
+cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                            const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z);
 
 }  // namespace wq

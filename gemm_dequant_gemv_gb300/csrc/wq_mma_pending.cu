@@ -1,12 +1,7 @@
-// Placeholder for the tensor-core paths until their kernels land.
+// Placeholder for the W8A8 path until its kernels land.
 #include "wq_mma.h"
 
 namespace wq {
-
-cudaError_t launch_wq4_mma(const void*, const int32_t*, const void*, const int32_t*, void*, int, int, int, int, int,
-                           unsigned, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 
 size_t w8a8_workspace_bytes(int M, int K, int N) {
   (void)N;

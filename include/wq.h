@@ -134,8 +134,10 @@ WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
  *   g_idx  int32 [K] with values in [0, K/group), or NULL
  *   y      act_dtype [M, N]
  *   act_dtype: WQ_F16 or WQ_BF16.  M >= 1; K % group == 0, group % 32 == 0;
- *   N % 8 == 0.  M <= 8 runs on CUDA cores; M >= 16 (no g_idx) on tcgen05
- *   tensor cores; other M return WQ_ERR_UNSUPPORTED in this build.
+ *   N % 8 == 0.  M <= 8 runs on CUDA cores (any g_idx).  M > 8 runs on the
+ *   tcgen05 tensor cores in chunks of up to 64 rows (padded to 16, 32 or 64)
+ *   and needs group % 64 == 0 and g_idx == NULL; otherwise it returns
+ *   WQ_ERR_UNSUPPORTED.
  *   workspace: none is needed; pass NULL and 0.
  */
 WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* scales,

@@ -108,8 +108,8 @@ def test_wq4_validation(wq):
     assert call(act=0) == wq.WQ_ERR_UNSUPPORTED   # not fp16 / bf16
     assert call(qz=MIS) == wq.WQ_ERR_ALIGN
     assert call(gi=MIS) == wq.WQ_ERR_ALIGN
-    assert call(M=12) == wq.WQ_ERR_UNSUPPORTED    # between the CUDA-core and tensor-core ranges
-    assert call(M=32, gi=A) == wq.WQ_ERR_UNSUPPORTED  # act-order is a CUDA-core path only
+    assert call(M=12, gi=A) == wq.WQ_ERR_UNSUPPORTED  # act-order is a CUDA-core path only (M <= 8)
+    assert call(M=32, g=32, K=256) == wq.WQ_ERR_UNSUPPORTED  # the tensor-core path needs group % 64
 
 
 def test_w8a8_validation(wq):

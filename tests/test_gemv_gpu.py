@@ -168,3 +168,38 @@ def test_repeat_bit_identical_and_pdl(G):
 def test_no_timeouts(G):
     import gemm_dequant_gemv_gb300 as wq
     assert wq.read_timeout_flag(clear=True) == 0
+
+
+# ------------------------------------------------------- tcgen05, M > 8 ----
+WQ4_MMA_CASES = [  # M, K, N, group, bf16, asym zeros
+    (16, 8192, 28672, 128, True, False), (32, 8192, 28672, 128, True, False),
+    (16, 256, 128, 64, True, False), (17, 512, 264, 128, False, True), (33, 1024, 392, 256, True, True),
+    (9, 2048, 1024, 128, False, False), (50, 1024, 520, 64, True, False), (100, 512, 256, 128, False, True)]
+
+
+@pytest.mark.parametrize("M,K,N,g,bf16,asym", WQ4_MMA_CASES)
+def test_wq4_mma_parity(G, M, K, N, g, bf16, asym):
+    d = _make_wq4(M, K, N, g, bf16, asym, seed=11)
+    y = G.run_wq4(d)
+    cols = None
+    if N > 4096:
+        r = np.random.default_rng(1)
+        cols = np.unique(np.concatenate([np.arange(0, 256), np.arange(N - 256, N), r.integers(0, N, 768)]))
+    y_ref, a = G.oracle_wq4(d, cols)
+    yv = G.to_f64(y)
+    _tol(yv if cols is None else yv[:, cols], y_ref, a)
+
+
+def test_wq4_mma_onehot_exact(G):
+    """One-hot rows of x through the tensor-core path return the dequantized weight rows
+    exactly (integer A operand, scale applied once in fp32)."""
+    import oracle
+    d = _make_wq4(16, 512, 264, 128, True, True, seed=12)
+    x = np.zeros((16, 512), np.float32)
+    for m, k in enumerate((0, 7, 8, 63, 64, 127, 128, 200, 255, 256, 300, 383, 384, 450, 510, 511)):
+        x[m, k] = 1.0
+    import synthetic as syn
+    d["x"] = syn.f32_to_bf16_bits(x)
+    y = G.bits_u16(G.run_wq4(d))
+    y_ref, _ = G.oracle_wq4(d)
+    assert np.array_equal(y, oracle.round_bf16(y_ref))
