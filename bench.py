@@ -75,6 +75,16 @@ def job_throughput(step_bytes: int, steps: int, world: int, max_ms: float) -> fl
     return step_bytes * steps * world / (max_ms * 1e-3) / 1e9
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (burst), TFLOP/s: the fp16/bf16 MMA rate the exact
+    integer product of the W8A8 path runs at."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # ----------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -206,8 +216,9 @@ def run_ours(args, rank, world, dev):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
         step(True)
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
+    with torch.cuda.stream(stream):  # CUDAGraph.replay() launches on the current stream
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
     torch.cuda.synchronize(dev)
 
     gpu_id = torch.cuda.get_device_properties(dev).uuid
@@ -218,10 +229,11 @@ def run_ours(args, rank, world, dev):
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id) as clk:
         torch.cuda.synchronize(dev)
-        t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        t1.record(stream)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            t1.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -341,6 +353,94 @@ def run_reference(args):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------- the other two workloads ----
+
+def _time_graph(graph, stream, reps, dev):
+    import torch
+    with torch.cuda.stream(stream):  # CUDAGraph.replay() launches on the current stream
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps  # ms per replay
+
+
+def run_wq4_sweep(args, dev):
+    """W4A16 (symmetric uint4, group 128, bf16) at K=8192, N=28672 for each M:
+    three weight copies (363 MB, larger than L2) cycled in one CUDA graph."""
+    import torch
+
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    peak, peak_kind = measured_peaks()
+    K, N, g = 8192, 28672, 128
+    base = syn.make_wq4_sym(seed=4, M=1, K=K, N=N, group=g)
+    copies = 3
+    qws = [to_dev(base["qweight"], dev) for _ in range(copies)]
+    scs = [to_dev(base["scales"], dev) for _ in range(copies)]
+    stream = torch.cuda.Stream(device=dev)
+    lines = []
+    for M in (1, 2, 4, 8, 16, 32):
+        x = to_dev(syn.f32_to_bf16_bits(syn.normal(4 + M, 1, (M, K))), dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            for c in range(copies):
+                wq.wq4_gemm(x, qws[c], scs[c], None, None, y, M, K, N, g, wq.WQ_BF16, flags=wq.WQ_FLAG_PDL,
+                            stream=stream)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        per = 8
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+            for r in range(per):
+                c = r % copies
+                wq.wq4_gemm(x, qws[c], scs[c], None, None, y, M, K, N, g, wq.WQ_BF16, flags=wq.WQ_FLAG_PDL,
+                            stream=stream)
+        ms = _time_graph(graph, stream, max(3, args.steps // 100), dev) / per
+        nbytes = (K // 8) * N * 4 + (K // g) * N * 2 + M * K * 2 + M * N * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        lines.append({"workload": f"W4A16 sym g128 K={K} N={N} M={M}", "M": M,
+                      "path": "tcgen05" if M > 8 else "cuda-core", "us_per_call": ms * 1e3,
+                      "achieved_GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": peak_kind,
+                      "tflops": 2 * M * K * N / (ms * 1e-3) / 1e12})
+    return lines
+
+
+def run_w8a8(args, dev):
+    """W8A8 dynamic-quantization GEMM at M=2048, K=N=8192 (quantization + GEMM per call)."""
+    import torch
+
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    M, K, N = 2048, 8192, 8192
+    d = syn.make_w8a8(seed=5, M=M, K=K, N=N)
+    X, W, Sw = to_dev(d["X"], dev), to_dev(d["W"], dev), to_dev(d["Sw"], dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    nbytes = wq.w8a8_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        wq.w8a8_gemm(X, W, Sw, Y, M, K, N, workspace=ws, workspace_bytes=nbytes, stream=stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    per = 4
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        for _ in range(per):
+            wq.w8a8_gemm(X, W, Sw, Y, M, K, N, workspace=ws, workspace_bytes=nbytes, flags=wq.WQ_FLAG_PDL,
+                         stream=stream)
+    ms = _time_graph(graph, stream, max(3, args.steps // 400), dev) / per
+    pk, pk_kind = measured_bf16_peak()
+    tf = 2 * M * K * N / (ms * 1e-3) / 1e12
+    return [{"workload": f"W8A8 dynamic quant GEMM M={M} K={K} N={N}", "us_per_call": ms * 1e3, "tops": tf,
+             "peak_tflops_f16_dense": pk, "peak_source": pk_kind, "frac_of_tensor_peak": tf / pk,
+             "note": "exact int8 products on fp16 tcgen05 MMA; the int8 legacy mma.sync path measured 158 TOPS"}]
+
+
 # -------------------------------------------------------------------- main ----
 
 def main():
@@ -352,6 +452,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds of oracle work the reference arm aims for")
+    ap.add_argument("--workload", default="gemv_step", choices=["gemv_step", "wq4_sweep", "w8a8"],
+                    help="gemv_step is the headline; the others print one extra line per case")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -366,6 +468,12 @@ def main():
 
     import torch
     dev = torch.device(f"cuda:{local}")
+    if args.workload != "gemv_step":
+        torch.cuda.set_device(dev)
+        fn = run_wq4_sweep if args.workload == "wq4_sweep" else run_w8a8
+        for ln in fn(args, dev):
+            print(json.dumps(ln), flush=True)
+        return
     if world > 1:
         torch.cuda.set_device(dev)
         torch.distributed.init_process_group("nccl", device_id=dev)

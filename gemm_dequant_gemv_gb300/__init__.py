@@ -30,6 +30,8 @@ SIGNATURES = {
     "wq8_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _U, _P]),
     "wq3_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _U, _P]),
     "wq4_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _U, _P]),
+    "wq4_actorder_prepare": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "wq4_gemm_sorted": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _U, _P]),
     "w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _U, _P]),
     "w8a8_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
 }
@@ -111,6 +113,18 @@ def wq4_gemm(x, qweight, scales, qzeros, g_idx, y, M, K, N, group_size, act_dtyp
     _check("wq4_gemm", _lib.wq4_gemm(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx),
                                      _ptr(y), M, K, N, group_size, act_dtype, _ptr(workspace),
                                      workspace_bytes, flags, _stream(stream)))
+
+
+def wq4_actorder_prepare(qweight, g_idx, K, N, group_size, qweight_sorted, perm, stream=None):
+    _check("wq4_actorder_prepare", _lib.wq4_actorder_prepare(_ptr(qweight), _ptr(g_idx), K, N, group_size,
+                                                             _ptr(qweight_sorted), _ptr(perm), _stream(stream)))
+
+
+def wq4_gemm_sorted(x, qweight_sorted, scales, qzeros, perm, y, M, K, N, group_size, act_dtype, flags=0,
+                    stream=None):
+    _check("wq4_gemm_sorted", _lib.wq4_gemm_sorted(_ptr(x), _ptr(qweight_sorted), _ptr(scales), _ptr(qzeros),
+                                                   _ptr(perm), _ptr(y), M, K, N, group_size, act_dtype, flags,
+                                                   _stream(stream)))
 
 
 def w8a8_gemm_workspace_bytes(M, K, N) -> int:

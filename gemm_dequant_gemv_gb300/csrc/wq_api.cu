@@ -175,13 +175,14 @@ WQ_API wq_status wq8_gemv(const float* x, const int8_t* w, const float* scales, 
   if (group_size < 16 || group_size % 16 != 0 || K % group_size != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(y)) return WQ_ERR_ALIGN;
 
-  const int T = (N + 127) / 128, units = K / 8;
+  const int T = (N + 127) / 128, units = K / 16;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, nullptr, nullptr, M, K, N, group_size, 0};
-  a.ng_max = max_groups_per_slice(units, p.S, 8, group_size);
+  a.ng_max = max_groups_per_slice(units, p.S, 16, group_size);
   if (wq8_gemv_smem_bytes(p.MT, a.ng_max) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
   CUtensorMap wmap, xmap;
-  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 128, wq8_stage_k(),
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, K, M, 4, wq8_stage_k(), p.MT))
     return WQ_ERR_CUDA;
   return from_cuda(launch_wq8_gemv(p, wmap, xmap, a));
@@ -241,6 +242,41 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
       (act_order && !encode_x_map(&gmap, CU_TENSOR_MAP_DATA_TYPE_INT32, g_idx, K, 1, 4, wq4_stage_k(), 1)))
     return WQ_ERR_CUDA;
   return from_cuda(launch_wq4_gemv(p, wmap, xmap, act_order ? &gmap : nullptr, a, act_bf16, qzeros != nullptr));
+}
+
+WQ_API wq_status wq4_actorder_prepare(const int32_t* qweight, const int32_t* g_idx, int K, int N, int group_size,
+                                      int32_t* qweight_sorted, int32_t* perm, void* stream) {
+  if (!qweight || !g_idx || !qweight_sorted || !perm) return WQ_ERR_NULL;
+  if (K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 32 || group_size % 32 != 0 || K % group_size != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(qweight) || !aligned16(g_idx) || !aligned16(qweight_sorted) || !aligned16(perm)) return WQ_ERR_ALIGN;
+  const int r = actorder_prepare(qweight, g_idx, K, N, group_size, qweight_sorted, perm,
+                                 static_cast<cudaStream_t>(stream));
+  return r == 0 ? WQ_OK : (r == 1 ? WQ_ERR_SHAPE : WQ_ERR_CUDA);
+}
+
+WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, const void* scales,
+                                 const int32_t* qzeros, const int32_t* perm, void* y, int M, int K, int N,
+                                 int group_size, int act_dtype, unsigned flags, void* stream) {
+  if (!x || !qweight_sorted || !scales || !perm || !y) return WQ_ERR_NULL;
+  if (M < 1 || M > 8 || K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 32 || group_size % 32 != 0 || K % group_size != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (act_dtype != WQ_F16 && act_dtype != WQ_BF16) return WQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qweight_sorted) || !aligned16(scales) || !aligned16(perm) || !aligned16(y) ||
+      (qzeros && !aligned16(qzeros)))
+    return WQ_ERR_ALIGN;
+  const int T = (N + 127) / 128, units = K / 32;
+  LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
+  GemvArgs a{x, y, scales, qzeros, nullptr, M, K, N, group_size, 0};
+  a.ng_max = max_groups_per_slice(units, p.S, 32, group_size);
+  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, false, 0, size_t(p.MT) * K * 2) > static_cast<size_t>(device_max_smem()))
+    return WQ_ERR_UNSUPPORTED;
+  CUtensorMap wmap, pmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight_sorted, N, K / 8, size_t(N) * 4, 128, 32,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_x_map(&pmap, CU_TENSOR_MAP_DATA_TYPE_INT32, perm, K, 1, 4, wq4_stage_k(), 1))
+    return WQ_ERR_CUDA;
+  return from_cuda(launch_wq4_gemv(p, wmap, pmap, nullptr, a, act_dtype == WQ_BF16, qzeros != nullptr, true));
 }
 
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N) { return w8a8_workspace_bytes(M, K, N); }

@@ -113,25 +113,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     pdl_wait();
     const uint32_t magic = 0x3F000000u;
 
+    float2* xcw = xc + warp * 32;
     for (int it = 0; it < n_loads; ++it) {
       const int s = it % kNS;
       const int u = u0 + it * kConsumerWarps + warp;
       if (!mbar_wait(&full[s], (it / kNS) & 1)) *cfailed = 1;
-      consumer_sync(kConsumerThreads);
       if (*cfailed) break;
       {
-        const __half* xr = reinterpret_cast<const __half*>(xst + size_t(s) * kXBytes);
+        const __half* xr = reinterpret_cast<const __half*>(xst + size_t(s) * kXBytes) + warp * 32 + lane;
         const bool live = u < u1;  // k = 32u + lane belongs to this CTA's range
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const float v = live ? __half2float(xr[m * kStageK + tid]) : 0.f;
+          const float v = live ? __half2float(xr[m * kStageK]) : 0.f;
           const float xp = v * fac;
-          xc[m * kStageK + tid] = make_float2(xp, xp);
+          xcw[m * kStageK + lane] = make_float2(xp, xp);
           bsum[m] = fmaf(v, bfac, bsum[m]);
           xsum[m] += v;
         }
       }
-      consumer_sync(kConsumerThreads);
+      __syncwarp();
       if (u < u1) {
         const uint8_t* rowp = wst + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
         const uint4 A = *reinterpret_cast<const uint4*>(rowp);
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           t[c][7] = w2[c] >> 3;
           t[c][8] = w2[c] >> 15;
         }
-        const float4* xw = reinterpret_cast<const float4*>(xc) + warp * 16;
+        const float4* xw = reinterpret_cast<const float4*>(xcw);
 #pragma unroll
         for (int jp = 0; jp < 16; ++jp) {
           float4 xq[MT];

@@ -32,16 +32,19 @@ __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(
 
 // Shared-memory carve-up (same arithmetic on host and device).
 struct Smem4 {
-  size_t xst, xc, aux, zw, part, bars, flag, total;
-  __host__ __device__ Smem4(int MT, int ng_max, bool act_order, int G) {
+  size_t xst, xc, aux, zw, xfull, part, bars, flag, total;
+  // xfull_bytes: the whole x (MT rows of K values) for the permuted variant, else 0
+  __host__ __device__ Smem4(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes = 0) {
     size_t o = size_t(kNS) * kStageBytes;
-    xst = o;  o = align16(o + size_t(kNS) * MT * kStageK * 2);            // raw x per stage (+ g_idx)
+    // raw x (or the perm slice of the sorted variant) per stage, then g_idx per stage for act-order
+    xst = o;  o = align16(o + size_t(kNS) * (MT * kStageK * 2 > kStageK * 4 ? MT * kStageK * 2 : kStageK * 4));
     if (act_order) o = align16(o + size_t(kNS) * kStageK * 4);
     xc = o;   o = align16(o + size_t(MT) * kStageK * 8);                  // converted x pairs
     aux = o;  // contiguous: raw 16-bit scales [ng_max][BN]; act-order: goff [256] + sd [G][2][32][4] floats
     if (act_order) o = align16(o + size_t(kStageK) * 4 + size_t(G) * kBN * 8);
     else           o = align16(o + size_t(ng_max) * kBN * 2);
     zw = o;   o = align16(o + (act_order ? 0 : size_t(ng_max) * (kBN / 8) * 4));
+    xfull = o; o = align16(o + xfull_bytes);
     part = o; o = align16(o + size_t(MT) * kBN * 4);
     bars = o; o = align16(o + size_t(2 * kNS) * 8);
     flag = o; o = align16(o + 16);
@@ -88,14 +91,18 @@ __device__ __forceinline__ void unit_row_accumulate(uint4 wd, const float4* xrow
 }
 
 // ---------------------------------------------------------------------------
-// Contiguous groups (g(k) = k / group).
+// Contiguous groups (g(k) = k / group).  PERM: the weight rows were sorted by
+// act-order group once ahead of time (wq4_actorder_prepare); row i of the
+// sorted weights multiplies x[perm[i]].  The whole x then sits in shared
+// memory and each stage brings the slice of perm (TMA box of the "x" map).
 // ---------------------------------------------------------------------------
-template <int MT, int ACT_BF16, bool HAS_Z>
+template <int MT, int ACT_BF16, bool HAS_Z, bool PERM>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     k4_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Smem4 L(MT, a.ng_max, false, 0);
+  const Smem4 L(MT, a.ng_max, false, 0, PERM ? size_t(MT) * a.K * 2 : 0);
+  const uint16_t* xfull = reinterpret_cast<const uint16_t*>(smem + L.xfull);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
@@ -131,8 +138,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   if (warp == kConsumerWarps) {
     int issued = 0;
     if (lane == 0 && n_loads > 0)
-      issued = produce_stages<kNS>(&wmap, &xmap, wst, kStageBytes, xst, MT * kStageK * 2, full, empty, n0, 4 * u0,
-                                   kStageRows, 32 * u0, kStageK, n_loads, failed);
+      issued = produce_stages<kNS>(&wmap, &xmap, wst, kStageBytes, xst, PERM ? kStageK * 4 : MT * kStageK * 2, full,
+                                   empty, n0, 4 * u0, kStageRows, 32 * u0, kStageK, n_loads, failed);
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
   } else {
@@ -153,35 +160,51 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       }
     }
     pdl_wait();
+    consumer_sync(kConsumerThreads);  // the scale and zero tables are complete before any warp folds
+    if (PERM) {  // the whole x in shared memory (rows >= M read as zero)
+      uint4* xf = reinterpret_cast<uint4*>(smem + L.xfull);
+      const int chunks_per_row = K / 8;
+      for (int i = tid; i < MT * chunks_per_row; i += kConsumerThreads) {
+        const int m = i / chunks_per_row, c = i % chunks_per_row;
+        xf[i] = (m < M) ? reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + size_t(m) * K)[c]
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+      consumer_sync(kConsumerThreads);
+    }
 
     float2 acc[MT][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
 
+    float2* xcw = xc + warp * 32;  // this warp's x pairs: [MT][stride kStageK]
     for (int it = 0; it < n_loads; ++it) {
       const int s = it % kNS;
       const int u = u0 + it * kConsumerWarps + warp;
       if (!mbar_wait(&full[s], (it / kNS) & 1)) *cfailed = 1;
-      consumer_sync(kConsumerThreads);  // previous stage's x pairs are no longer read
       if (*cfailed) break;
-      // convert this stage's x: thread tid handles k = tid (its own warp's unit) for every row
+      // convert this warp's 32 values of x (one per lane, every row)
       float xu[MT];
       {
-        const uint16_t* xr = reinterpret_cast<const uint16_t*>(xst + size_t(s) * MT * kStageK * 2);
+        const uint16_t* xr = reinterpret_cast<const uint16_t*>(xst + size_t(s) * MT * kStageK * 2) + warp * 32 + lane;
+        int kp = 0;
+        if (PERM) {
+          kp = reinterpret_cast<const int32_t*>(xst + size_t(s) * kStageK * 4)[warp * 32 + lane];
+          kp = min(max(kp, 0), K - 1);  // out-of-range entries are clamped, never read out of bounds
+        }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const float v = act_to_f32<ACT_BF16>(xr[m * kStageK + tid]);
-          xc[m * kStageK + tid] = make_float2(v * 256.f, v * 256.f);
+          const float v = act_to_f32<ACT_BF16>(PERM ? xfull[size_t(m) * K + kp] : xr[m * kStageK]);
+          xcw[m * kStageK + lane] = make_float2(v * 256.f, v * 256.f);
           xu[m] = warp_sum(v);  // X_u of this warp's unit
         }
       }
-      consumer_sync(kConsumerThreads);
+      __syncwarp();
       if (u < u1) {
         float2 accg[MT][2];
 #pragma unroll
         for (int m = 0; m < MT; ++m) accg[m][0] = accg[m][1] = make_float2(0.f, 0.f);
         const uint8_t* rowp = wst + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
-        const float4* xw = reinterpret_cast<const float4*>(xc) + warp * 16;
+        const float4* xw = reinterpret_cast<const float4*>(xcw);
 #pragma unroll
         for (int i = 0; i < kUnitRows; ++i)
           unit_row_accumulate<MT>(*reinterpret_cast<const uint4*>(rowp + i * (kBN * 4)), xw + 4 * i, accg);
@@ -244,7 +267,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const Smem4 L(MT, 0, true, G);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
-  uint8_t* gst = xst + size_t(kNS) * MT * kStageK * 2;                // g_idx per stage
+  uint8_t* gst = smem + L.xst + size_t(kNS) * (MT * kStageK * 2 > kStageK * 4 ? MT * kStageK * 2 : kStageK * 4);
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
   uint32_t* goff = reinterpret_cast<uint32_t*>(smem + L.aux);        // [256] byte offsets of sd rows
   uint8_t* sd = smem + L.aux + size_t(kStageK) * 4;                  // [G][2 halves][32 lanes] x float4
@@ -330,34 +353,36 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       reinterpret_cast<float4*>(sd)[i] = v;
     }
     pdl_wait();
+    consumer_sync(kConsumerThreads);  // the table is complete before any warp gathers from it
 
     float2 acc[MT][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
     const uint32_t sd_lane = smem_u32(sd) + lane * 16;
 
+    float2* xcw = xc + warp * 32;
+    uint32_t* gw_own = goff + warp * 32;
     for (int it = 0; it < n_loads; ++it) {
       const int s = it % kNS;
       const int u = u0 + it * kConsumerWarps + warp;
       if (!mbar_wait(&full[s], (it / kNS) & 1)) *cfailed = 1;
-      consumer_sync(kConsumerThreads);
       if (*cfailed) break;
       {
-        const uint16_t* xr = reinterpret_cast<const uint16_t*>(xst + size_t(s) * kXBytes);
+        const uint16_t* xr = reinterpret_cast<const uint16_t*>(xst + size_t(s) * kXBytes) + warp * 32 + lane;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const float v = act_to_f32<ACT_BF16>(xr[m * kStageK + tid]) * 256.f;
-          xc[m * kStageK + tid] = make_float2(v, v);
+          const float v = act_to_f32<ACT_BF16>(xr[m * kStageK]) * 256.f;
+          xcw[m * kStageK + lane] = make_float2(v, v);
         }
-        int g = reinterpret_cast<const int32_t*>(gst + size_t(s) * kGBytes)[tid];
+        int g = reinterpret_cast<const int32_t*>(gst + size_t(s) * kGBytes)[warp * 32 + lane];
         g = min(max(g, 0), G - 1);  // out-of-range group indices are clamped, never read out of bounds
-        goff[tid] = uint32_t(g) * (kBN * 8);
+        gw_own[lane] = uint32_t(g) * (kBN * 8);
       }
-      consumer_sync(kConsumerThreads);
+      __syncwarp();
       if (u < u1) {
         const uint8_t* rowp = wst + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * (kBN * 4) + lane * 16;
-        const float4* xw = reinterpret_cast<const float4*>(xc) + warp * 16;
-        const uint4* gw = reinterpret_cast<const uint4*>(goff) + warp * 8;
+        const float4* xw = reinterpret_cast<const float4*>(xcw);
+        const uint4* gw = reinterpret_cast<const uint4*>(gw_own);
 #pragma unroll
         for (int i = 0; i < kUnitRows; ++i) {
           const uint4 wd = *reinterpret_cast<const uint4*>(rowp + i * (kBN * 4));
@@ -423,41 +448,43 @@ cudaError_t launch3(const void* kern, const LaunchPlan& p, size_t smem, const CU
   return launch_gemv_kernel(kern, p, smem, maps, g ? 3 : 2, a);
 }
 
-template <int MT, int ACT, bool HZ, bool AO>
+// mode 0: contiguous groups, 1: act-order gather (g = g_idx map), 2: sorted rows (x = perm map)
+template <int MT, int ACT, bool HZ>
 cudaError_t launch_one(const LaunchPlan& p, const CUtensorMap& w, const CUtensorMap& x, const CUtensorMap* g,
-                       const GemvArgs& a) {
-  const Smem4 L(MT, a.ng_max, AO, a.K / a.group);
-  if (AO) return launch3(reinterpret_cast<const void*>(k4g_gemv_kernel<MT, ACT, HZ>), p, L.total, w, x, g, a);
-  return launch3(reinterpret_cast<const void*>(k4_gemv_kernel<MT, ACT, HZ>), p, L.total, w, x, nullptr, a);
+                       const GemvArgs& a, int mode) {
+  if (mode == 1)
+    return launch3(reinterpret_cast<const void*>(k4g_gemv_kernel<MT, ACT, HZ>), p,
+                   Smem4(MT, a.ng_max, true, a.K / a.group).total, w, x, g, a);
+  if (mode == 2)
+    return launch3(reinterpret_cast<const void*>(k4_gemv_kernel<MT, ACT, HZ, true>), p,
+                   Smem4(MT, a.ng_max, false, 0, size_t(MT) * a.K * 2).total, w, x, nullptr, a);
+  return launch3(reinterpret_cast<const void*>(k4_gemv_kernel<MT, ACT, HZ, false>), p,
+                 Smem4(MT, a.ng_max, false, 0).total, w, x, nullptr, a);
 }
 
 template <int MT>
 cudaError_t dispatch_act(const LaunchPlan& p, const CUtensorMap& w, const CUtensorMap& x, const CUtensorMap* g,
-                         const GemvArgs& a, int act_bf16, bool has_z) {
-  const bool ao = g != nullptr;
-  if (act_bf16) {
-    if (has_z) return ao ? launch_one<MT, 1, true, true>(p, w, x, g, a) : launch_one<MT, 1, true, false>(p, w, x, g, a);
-    return ao ? launch_one<MT, 1, false, true>(p, w, x, g, a) : launch_one<MT, 1, false, false>(p, w, x, g, a);
-  }
-  if (has_z) return ao ? launch_one<MT, 0, true, true>(p, w, x, g, a) : launch_one<MT, 0, true, false>(p, w, x, g, a);
-  return ao ? launch_one<MT, 0, false, true>(p, w, x, g, a) : launch_one<MT, 0, false, false>(p, w, x, g, a);
+                         const GemvArgs& a, int act_bf16, bool has_z, int mode) {
+  if (act_bf16) return has_z ? launch_one<MT, 1, true>(p, w, x, g, a, mode) : launch_one<MT, 1, false>(p, w, x, g, a, mode);
+  return has_z ? launch_one<MT, 0, true>(p, w, x, g, a, mode) : launch_one<MT, 0, false>(p, w, x, g, a, mode);
 }
 
 }  // namespace
 
-size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G) {
-  return Smem4(MT, ng_max, act_order, G).total;
+size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes) {
+  return Smem4(MT, ng_max, act_order, G, xfull_bytes).total;
 }
 
 int wq4_stage_k() { return kStageK; }
 
 cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                            const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z) {
+                            const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z, bool sorted) {
+  const int mode = gmap ? 1 : (sorted ? 2 : 0);
   switch (p.MT) {
-    case 1: return dispatch_act<1>(p, wmap, xmap, gmap, a, act_bf16, has_z);
-    case 2: return dispatch_act<2>(p, wmap, xmap, gmap, a, act_bf16, has_z);
-    case 4: return dispatch_act<4>(p, wmap, xmap, gmap, a, act_bf16, has_z);
-    case 8: return dispatch_act<8>(p, wmap, xmap, gmap, a, act_bf16, has_z);
+    case 1: return dispatch_act<1>(p, wmap, xmap, gmap, a, act_bf16, has_z, mode);
+    case 2: return dispatch_act<2>(p, wmap, xmap, gmap, a, act_bf16, has_z, mode);
+    case 4: return dispatch_act<4>(p, wmap, xmap, gmap, a, act_bf16, has_z, mode);
+    case 8: return dispatch_act<8>(p, wmap, xmap, gmap, a, act_bf16, has_z, mode);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,11 +17,11 @@ namespace wq {
 namespace {
 
 constexpr int kBN = 128;           // int8 columns per tile: one 128-byte row per warp
-constexpr int kUnitRows = 8;       // rows (= values of k) per consumer unit
+constexpr int kUnitRows = 16;      // rows (= values of k) per consumer unit
 constexpr int kStageRows = kConsumerWarps * kUnitRows;
-constexpr int kStageK = kStageRows;            // 64 values of k per stage
-constexpr int kStageBytes = kStageRows * kBN;  // 8 KB
-constexpr int kNS = 8;
+constexpr int kStageK = kStageRows;            // 128 values of k per stage
+constexpr int kStageBytes = kStageRows * kBN;  // 16 KB
+constexpr int kNS = 4;
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -94,29 +94,38 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       reinterpret_cast<float4*>(scl)[i] = v;
     }
     pdl_wait();
+    consumer_sync(kConsumerThreads);  // the scale table is complete before any warp folds
 
     float2 acc[MT][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
     const float2 unbias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
 
+    float2* xcw = xc + warp * kUnitRows;
     for (int it = 0; it < n_loads; ++it) {
       const int s = it % kNS;
       const int u = u0 + it * kConsumerWarps + warp;
       if (!mbar_wait(&full[s], (it / kNS) & 1)) *cfailed = 1;
-      consumer_sync(kConsumerThreads);
       if (*cfailed) break;
       {
-        const float* xr = reinterpret_cast<const float*>(xst + size_t(s) * kXBytes);
-        for (int e = tid; e < MT * kStageK; e += kConsumerThreads) xc[e] = make_float2(xr[e], xr[e]);
+        // this warp's 16 values of x for every row: lane -> (m, j) = (lane / 16 + 2 r, lane % 16)
+        const float* xr = reinterpret_cast<const float*>(xst + size_t(s) * kXBytes) + warp * kUnitRows;
+#pragma unroll
+        for (int r = 0; r < (MT * kUnitRows + 31) / 32; ++r) {
+          const int m = lane / kUnitRows + r * (32 / kUnitRows), j = lane % kUnitRows;
+          if (m < MT) {
+            const float v = xr[m * kStageK + j];
+            xcw[m * kStageK + j] = make_float2(v, v);
+          }
+        }
       }
-      consumer_sync(kConsumerThreads);
+      __syncwarp();
       if (u < u1) {
         float2 accg[MT][2];
 #pragma unroll
         for (int m = 0; m < MT; ++m) accg[m][0] = accg[m][1] = make_float2(0.f, 0.f);
         const uint8_t* rowp = wst + size_t(s) * kStageBytes + size_t(warp * kUnitRows) * kBN + lane * 4;
-        const float4* xw = reinterpret_cast<const float4*>(xc) + warp * (kUnitRows / 2);
+        const float4* xw = reinterpret_cast<const float4*>(xcw);
 #pragma unroll
         for (int jp = 0; jp < kUnitRows / 2; ++jp) {
           float4 xq[MT];

@@ -28,7 +28,7 @@ cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t sme
 
 size_t wq8_gemv_smem_bytes(int MT, int ng_max);
 size_t wq3_gemv_smem_bytes(int MT);
-size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G);
+size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes = 0);
 
 // Values of k one pipeline stage covers (the x box width of each kernel).
 int wq8_stage_k();
@@ -39,8 +39,10 @@ cudaError_t launch_wq8_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const 
                             const GemvArgs& a);
 cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                             const GemvArgs& a);
-// gmap != nullptr selects the act-order kernel (g_idx staged per stage).
+// gmap != nullptr selects the act-order kernel (g_idx staged per stage);
+// sorted selects the kernel for group-sorted rows, with xmap mapping perm.
 cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                            const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z);
+                            const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z,
+                            bool sorted = false);
 
 }  // namespace wq

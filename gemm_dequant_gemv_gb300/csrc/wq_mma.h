@@ -19,4 +19,9 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
                         int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
                         cudaStream_t stream);
 
+// Act-order preparation (host-driven, synchronous on `stream`): 0 = ok,
+// 1 = g_idx is not a grouping with exactly `group` rows per group, 2 = CUDA error.
+int actorder_prepare(const int32_t* qweight, const int32_t* g_idx, int K, int N, int group, int32_t* qweight_sorted,
+                     int32_t* perm, cudaStream_t stream);
+
 }  // namespace wq

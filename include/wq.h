@@ -147,6 +147,38 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
                           unsigned flags, void* stream);
 
 /*
+ * wq4_actorder_prepare -- one-time preparation of act-order 4-bit weights for
+ * wq4_gemm_sorted: sorts the rows of qweight by group, stable in k, so that
+ * every group becomes a contiguous run of `group_size` rows.
+ * [QC] Int4 Weight Only Quantization (group-wise); the act_order option of the
+ *      GPTQ configuration (GPTQ算法解析, 4.1 内存-计算权衡).
+ *   qweight        int32 [K/8, N]  input (device)
+ *   g_idx          int32 [K]       input (device); every group must hold
+ *                                  exactly group_size rows, else WQ_ERR_SHAPE
+ *   qweight_sorted int32 [K/8, N]  output (device): sorted row i = row perm[i]
+ *   perm           int32 [K]       output (device); g_idx[perm[i]] == i / group_size
+ * Synchronous on `stream` (it reads g_idx back to the host); not for a hot path.
+ */
+WQ_API wq_status wq4_actorder_prepare(const int32_t* qweight, const int32_t* g_idx, int K, int N,
+                                      int group_size, int32_t* qweight_sorted, int32_t* perm,
+                                      void* stream);
+
+/*
+ * wq4_gemm_sorted -- the act-order GEMV on weights prepared by
+ * wq4_actorder_prepare:
+ *   y[m,n] = sum_i x[m, perm[i]] * scales[i/group, n] * (qs(i,n) - z(i/group, n))
+ * which equals wq4_gemm with g_idx on the original weights (same scales and
+ * qzeros: group ids do not change).  Each group is contiguous, so one scale
+ * and zero apply per group instead of per code.
+ *   1 <= M <= 8; K % group == 0, group % 32 == 0; N % 8 == 0; x (M*K values)
+ *   must fit in shared memory next to the pipeline (M * K * 2 bytes <= about
+ *   96 KB), else WQ_ERR_UNSUPPORTED.  Other arguments as in wq4_gemm.
+ */
+WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, const void* scales,
+                                 const int32_t* qzeros, const int32_t* perm, void* y, int M, int K,
+                                 int N, int group_size, int act_dtype, unsigned flags, void* stream);
+
+/*
  * w8a8_gemm -- W8A8 dynamic-quantization GEMM.
  *   Sx[m]    = fp32(max_k |X[m,k]| / 127)              (fp32 division)
  *   Xq[m,k]  = clamp(rint(fp32(X[m,k] / Sx[m])), -127, 127)   (ties to even;

@@ -19,9 +19,9 @@ def G():
     return gpu_util
 
 
-def _tol(y, y_ref, a):
-    from tolerance import within
-    ok, worst = within(y, y_ref, a)
+def _tol(y, y_ref, a, out="f32"):
+    from tolerance import unit_roundoff, within
+    ok, worst = within(y, y_ref, a, unit_roundoff(out))
     assert ok, f"max |err|/bound = {worst:.3g}"
     return worst
 
@@ -66,7 +66,7 @@ def test_wq3_parity(G, M, K, N):
     y = G.run_wq3(d)
     y_ref, a = oracle.wq3_gemv(d["x"].view(np.uint16), d["mat"], d["scales"].view(np.uint16),
                                d["zeros"].view(np.uint16))
-    _tol(G.to_f64(y), y_ref, a)
+    _tol(G.to_f64(y), y_ref, a, "f16")
 
 
 def test_wq3_onehot_exact(G):
@@ -118,7 +118,7 @@ def test_wq4_parity(G, M, K, N, g, bf16, asym):
         cols = np.unique(np.concatenate([np.arange(0, 256), np.arange(N - 256, N), r.integers(0, N, 1024)]))
     y_ref, a = G.oracle_wq4(d, cols)
     yv = G.to_f64(y)
-    _tol(yv if cols is None else yv[:, cols], y_ref, a)
+    _tol(yv if cols is None else yv[:, cols], y_ref, a, "bf16" if bf16 else "f16")
 
 
 WQ4G_CASES = [(1, 256, 128, 32), (1, 1024, 392, 128), (4, 2048, 1024, 64), (1, 4096, 11008, 128),
@@ -131,7 +131,7 @@ def test_wq4_actorder_parity(G, M, K, N, g):
     d = syn.make_wq4_actorder(seed=3, M=M, K=K, N=N, group=g)
     y = G.run_wq4(d)
     y_ref, a = G.oracle_wq4(d)
-    _tol(G.to_f64(y), y_ref, a)
+    _tol(G.to_f64(y), y_ref, a, "f16")
 
 
 @pytest.mark.parametrize("act_order", [False, True])
@@ -187,7 +187,7 @@ def test_wq4_mma_parity(G, M, K, N, g, bf16, asym):
         cols = np.unique(np.concatenate([np.arange(0, 256), np.arange(N - 256, N), r.integers(0, N, 768)]))
     y_ref, a = G.oracle_wq4(d, cols)
     yv = G.to_f64(y)
-    _tol(yv if cols is None else yv[:, cols], y_ref, a)
+    _tol(yv if cols is None else yv[:, cols], y_ref, a, "bf16" if bf16 else "f16")
 
 
 def test_wq4_mma_onehot_exact(G):
@@ -203,3 +203,45 @@ def test_wq4_mma_onehot_exact(G):
     y = G.bits_u16(G.run_wq4(d))
     y_ref, _ = G.oracle_wq4(d)
     assert np.array_equal(y, oracle.round_bf16(y_ref))
+
+
+# ------------------------------------------- act-order on group-sorted rows ----
+WQ4S_CASES = [(1, 256, 128, 32), (1, 4096, 11008, 128), (3, 2048, 1032, 64), (8, 1024, 256, 128)]
+
+
+@pytest.mark.parametrize("M,K,N,g", WQ4S_CASES)
+def test_wq4_sorted_matches_actorder_oracle(G, M, K, N, g):
+    """Prepared (row-sorted) weights + perm reproduce the act-order product of the
+    original weights and g_idx; the repack itself is checked bit for bit."""
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    d = syn.make_wq4_actorder(seed=13, M=M, K=K, N=N, group=g)
+    qw, gi = G.dev(d["qweight"]), G.dev(d["g_idx"])
+    qs = torch.empty_like(qw)
+    perm = torch.empty_like(gi)
+    wq.wq4_actorder_prepare(qw, gi, K, N, g, qs, perm)
+    p = perm.cpu().numpy()
+    assert np.array_equal(np.sort(p), np.arange(K))
+    assert np.array_equal(d["g_idx"][p], np.arange(K) // g)
+    assert np.array_equal(qs.cpu().numpy(), syn.pack4(d["codes"][p]))
+    x, sc, qz = G.dev(d["x"]), G.dev(d["scales"]), G.dev(d["qzeros"])
+    buf, y = G.guarded((M, N), torch.float16)
+    wq.wq4_gemm_sorted(x, qs, sc, qz, perm, y, M, K, N, g, wq.WQ_F16)
+    torch.cuda.synchronize()
+    G.check_canary(buf, M * N)
+    y_ref, a = G.oracle_wq4(d)
+    _tol(G.to_f64(y), y_ref, a, "f16")
+
+
+def test_wq4_prepare_rejects_unequal_groups(G):
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    K, N, g = 256, 128, 64
+    gi = np.repeat(np.arange(K // g), g).astype(np.int32)
+    gi[0], gi[-1] = 1, 1   # group 0 loses a row, group 1 gains one
+    qw = torch.zeros((K // 8, N), dtype=torch.int32, device=G.DEV)
+    qs, perm = torch.empty_like(qw), torch.empty(K, dtype=torch.int32, device=G.DEV)
+    with pytest.raises(wq.WQError) as e:
+        wq.wq4_actorder_prepare(qw, G.dev(gi), K, N, g, qs, perm)
+    assert e.value.status == wq.WQ_ERR_SHAPE

@@ -1,0 +1,89 @@
+"""GPU parity of the W8A8 dynamic-quantization GEMM against the oracle.
+
+The row quantization (Sx, Xq) and the int32 product are compared bit for bit;
+Y is compared under |y - y_ref| <= 1e-3 * sum_k |x_k w_kn| + 1e-5 + 2^-8 |y_ref|
+with x = Sx Xq and w = Sw Wq (the last term is the bf16 rounding of the stored
+output).  Shapes cover one and several 128 x 128 tiles, ragged M and N,
+a K that is not a multiple of the 256-value exact chunk, adversarial
+full-magnitude codes, an all-zero row, and the full 2048 x 8192 x 8192
+workload (every row's quantization, sampled rows of the product).
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    import gpu_util
+    return gpu_util
+
+
+def run_w8a8(G, X_bits, W, Sw, want_acc=True):
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    M, K = X_bits.shape
+    N = W.shape[1]
+    X, Wd, Swd = G.dev(X_bits), G.dev(W), G.dev(Sw)
+    buf, Y = G.guarded((M, N), torch.bfloat16)
+    Xq = torch.empty((M, K), dtype=torch.int8, device=G.DEV)
+    Sx = torch.empty((M,), dtype=torch.float32, device=G.DEV)
+    acc = torch.empty((M, N), dtype=torch.int32, device=G.DEV) if want_acc else None
+    ws_bytes = wq.w8a8_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=G.DEV)
+    wq.w8a8_gemm(X, Wd, Swd, Y, M, K, N, Xq, Sx, acc, ws, ws_bytes)
+    torch.cuda.synchronize()
+    G.check_canary(buf, M * N)
+    return (Y, Xq.cpu().numpy(), Sx.cpu().numpy(),
+            None if acc is None else acc.cpu().numpy().astype(np.int64))
+
+
+def _check(G, X_bits, W, Sw, rows=None):
+    import oracle
+    from tolerance import U_BF16, within
+    Y, Xq, Sx, acc = run_w8a8(G, X_bits, W, Sw)
+    Xq_ref, Sx_ref = oracle.w8a8_quant_rows(X_bits)
+    assert np.array_equal(Sx.view(np.uint32), Sx_ref.view(np.uint32)), "Sx differs"
+    assert np.array_equal(Xq, Xq_ref), "Xq differs"
+    acc_ref, y_ref, a, ovf = oracle.w8a8_gemm_rows(Xq_ref, Sx_ref, W, Sw, rows)
+    assert not ovf
+    r = np.arange(X_bits.shape[0]) if rows is None else np.asarray(rows)
+    assert np.array_equal(acc[r], acc_ref), "int32 accumulator differs"
+    ok, worst = within(G.to_f64(Y)[r], y_ref, a, U_BF16)
+    assert ok, f"max |err|/bound = {worst:.3g}"
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 256, 128), (200, 512, 272), (128, 320, 128), (300, 1024, 512)])
+def test_w8a8_parity_small(G, M, K, N):
+    import synthetic as syn
+    d = syn.make_w8a8(seed=5, M=M, K=K, N=N)
+    _check(G, d["X"], d["W"], d["Sw"])
+
+
+def test_w8a8_adversarial_full_magnitude(G):
+    """Every code +-127 with aligned signs: |acc| = K * 127^2 (132 M at K = 8192)."""
+    import synthetic as syn
+    M, K, N = 128, 8192, 256
+    Xf = np.full((M, K), 2.0, np.float32)
+    Xf[1::2] = -2.0                      # rows of alternating sign
+    Xf[5] = 0.0                          # an all-zero row
+    W = np.full((K, N), 127, np.int8)
+    W[:, 1::3] = -127
+    Sw = np.full((N,), 0.01, np.float32)
+    _check(G, syn.f32_to_bf16_bits(Xf), W, Sw)
+
+
+def test_w8a8_full_workload_sampled_rows(G):
+    import synthetic as syn
+    d = syn.make_w8a8(seed=5)
+    rows = [0, 1, 127, 128, 129, 1000, 1023, 1024, 2046, 2047]
+    _check(G, d["X"], d["W"], d["Sw"], rows)
+
+
+def test_w8a8_repeat_bit_identical(G):
+    import synthetic as syn
+    d = syn.make_w8a8(seed=6, M=256, K=1024, N=384)
+    y1 = G.bits_u16(run_w8a8(G, d["X"], d["W"], d["Sw"], want_acc=False)[0])
+    y2 = G.bits_u16(run_w8a8(G, d["X"], d["W"], d["Sw"], want_acc=False)[0])
+    assert np.array_equal(y1, y2)
