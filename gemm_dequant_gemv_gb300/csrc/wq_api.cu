@@ -179,7 +179,7 @@ WQ_API wq_status wq8_gemv(const float* x, const int8_t* w, const float* scales, 
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, nullptr, nullptr, M, K, N, group_size, 0};
   a.ng_max = max_groups_per_slice(units, p.S, 16, group_size);
-  if (wq8_gemv_smem_bytes(p.MT, a.ng_max) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
+  if (wq8_gemv_smem_bytes(p.MT, a.ng_max, p.S) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
   CUtensorMap wmap, xmap;
   if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, N, K, N, 128, wq8_stage_k(),
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -199,7 +199,7 @@ WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
   const int T = (N + 127) / 128, units = K / 32;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, zeros, nullptr, M, K, N, 0, 0};
-  if (wq3_gemv_smem_bytes(p.MT) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
+  if (wq3_gemv_smem_bytes(p.MT, p.S) > static_cast<size_t>(device_max_smem())) return WQ_ERR_UNSUPPORTED;
   CUtensorMap wmap, xmap;
   if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat, N, 3 * (K / 32), size_t(N) * 4, 128, 24,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -233,7 +233,7 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
   GemvArgs a{x, y, scales, qzeros, g_idx, M, K, N, group_size, 0};
   const bool act_order = g_idx != nullptr;
   a.ng_max = act_order ? 1 : max_groups_per_slice(units, p.S, 32, group_size);
-  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, act_order, K / group_size) > static_cast<size_t>(device_max_smem()))
+  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, act_order, K / group_size, p.S) > static_cast<size_t>(device_max_smem()))
     return WQ_ERR_UNSUPPORTED;
   CUtensorMap wmap, xmap, gmap;
   if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, 128, 32,
@@ -269,7 +269,7 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, qzeros, nullptr, M, K, N, group_size, 0};
   a.ng_max = max_groups_per_slice(units, p.S, 32, group_size);
-  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, false, 0, size_t(p.MT) * K * 2) > static_cast<size_t>(device_max_smem()))
+  if (wq4_gemv_smem_bytes(p.MT, a.ng_max, false, 0, p.S, size_t(p.MT) * K * 2) > static_cast<size_t>(device_max_smem()))
     return WQ_ERR_UNSUPPORTED;
   CUtensorMap wmap, pmap;
   if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight_sorted, N, K / 8, size_t(N) * 4, 128, 32,

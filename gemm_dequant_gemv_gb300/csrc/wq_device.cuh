@@ -111,6 +111,46 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   return v;
 }
 
+// Arrive on this CTA's part of the cluster barrier without waiting (relaxed:
+// no memory ordering), and the matching wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
+// shared memory of CTA `rank` of the cluster (dst and bar are local
+// addresses, mapped to that CTA), completing on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst_local, const void* src, uint32_t bytes,
+                                                  uint32_t bar_local, uint32_t rank) {
+  const uint32_t dst = map_smem_to_rank(dst_local, rank);
+  const uint32_t bar = map_smem_to_rank(bar_local, rank);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk copy this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Asynchronous 16-byte store into the shared memory of CTA `rank` of the
+// cluster, counted (16 bytes) on that CTA's mbarrier.  dst and bar are this
+// CTA's addresses of the same variables.
+__device__ __forceinline__ void st_async_v4_to_rank(uint32_t dst_local, float a, float b, float c, float d,
+                                                    uint32_t bar_local, uint32_t rank) {
+  const uint32_t dst = map_smem_to_rank(dst_local, rank);
+  const uint32_t bar = map_smem_to_rank(bar_local, rank);
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+               : "memory");
+}
+
 // Named barrier among the consumer warps only (barrier 0 is __syncthreads).
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");

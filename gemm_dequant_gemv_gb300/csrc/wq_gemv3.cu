@@ -29,14 +29,13 @@ constexpr int kNS = 5;
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct Smem3 {
-  size_t xst, xc, red2, part, bars, flag, total;
-  __host__ __device__ explicit Smem3(int MT) {
+  size_t xst, xc, recv, bars, flag, total;
+  __host__ __device__ Smem3(int MT, int S) {
     size_t o = size_t(kNS) * kStageBytes;
     xst = o;  o = align16(o + size_t(kNS) * MT * kStageK * 2);
     xc = o;   o = align16(o + size_t(MT) * kStageK * 8);
-    red2 = o; o = align16(o + size_t(kConsumerWarps) * MT * 2 * 4);   // per-warp (B, X) sums
-    part = o; o = align16(o + size_t(MT) * kBN * 4);
-    bars = o; o = align16(o + size_t(2 * kNS) * 8);
+    recv = o; o = align16(o + TileReduce(S, kBN).recv_floats(MT) * 4);
+    bars = o; o = align16(o + size_t(2 * kNS + 1) * 8);
     flag = o; o = align16(o + 16);
     total = o;
   }
@@ -59,14 +58,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     k3_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Smem3 L(MT);
+  const Smem3 L(MT, gridDim.x);
+  const TileReduce R(gridDim.x, kBN);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
-  float* red2 = reinterpret_cast<float*>(smem + L.red2);
-  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
+  uint64_t* recv_bar = empty + kNS;
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);  // producer's
   volatile int* cfailed = failed + 1;                                       // consumers'
 
@@ -85,9 +85,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     *failed = 0;
     *cfailed = 0;
+    R.init_bar(recv_bar, MT, kBN);
     fence_mbar_init();
   }
   __syncthreads();
+  if (S > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
@@ -97,6 +99,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                                    kStageRows, 32 * u0, kStageK, n_loads, failed);
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
+    __syncwarp();
+    if (S > 1) cluster_wait();
   } else {
     const int tid = threadIdx.x;
     // this thread converts code position j = lane of every block it stages
@@ -179,44 +183,28 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // per-warp constants B and X (lane order is fixed, so the sums are deterministic)
+    // this warp's share of y: s (sum x' m - B_w) - zero X_w over the k it handled
+    // (B_w, X_w: butterfly sums over the lanes, the same value in every lane)
+    const __half* SC = static_cast<const __half*>(a.scales);
+    const __half* ZR = static_cast<const __half*>(a.zeros);
+    float sc[4], zr[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int n = n0 + 4 * lane + c;
+      sc[c] = n < N ? __half2float(SC[n]) : 0.f;
+      zr[c] = n < N ? __half2float(ZR[n]) : 0.f;
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       const float b = warp_sum(bsum[m]), x = warp_sum(xsum[m]);
-      if (lane == 0) {
-        red2[(warp * MT + m) * 2 + 0] = b;
-        red2[(warp * MT + m) * 2 + 1] = x;
-      }
+      acc[m][0] = make_float2(fmaf(sc[0], acc[m][0].x - b, -zr[0] * x), fmaf(sc[1], acc[m][0].y - b, -zr[1] * x));
+      acc[m][1] = make_float2(fmaf(sc[2], acc[m][1].x - b, -zr[2] * x), fmaf(sc[3], acc[m][1].y - b, -zr[3] * x));
     }
-    consumer_sync(kConsumerThreads);
-    float* red = reinterpret_cast<float*>(wst);
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-      *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
-          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-    consumer_sync(kConsumerThreads);
-    const __half* SC = static_cast<const __half*>(a.scales);
-    const __half* ZR = static_cast<const __half*>(a.zeros);
-    for (int e = tid; e < MT * kBN; e += kConsumerThreads) {
-      const int m = e / kBN, col = e % kBN, n = n0 + col;
-      float v = 0.f, Bm = 0.f, Xm = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        v += red[(w * MT + m) * kBN + col];
-        Bm += red2[(w * MT + m) * 2 + 0];
-        Xm += red2[(w * MT + m) * 2 + 1];
-      }
-      float r = 0.f;
-      if (n < N) {
-        const float sc = __half2float(SC[n]), zr = __half2float(ZR[n]);
-        r = fmaf(sc, v - Bm, -zr * Xm);
-      }
-      part[e] = r;
-    }
+    push_partials<MT, kBN>(R, acc, recv, recv_bar, warp, lane);
   }
 
   __half* Y = static_cast<__half*>(a.y);
-  finish_tile<MT, kBN>(part, S, [&](int m, int col, float v) {
+  owner_reduce_store<MT, kBN>(R, recv, recv_bar, [&](int m, int col, float v) {
     const int n = n0 + col;
     if (m < M && n < N) Y[size_t(m) * N + n] = __float2half_rn(v);
   });
@@ -224,7 +212,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
 }  // namespace
 
-size_t wq3_gemv_smem_bytes(int MT) { return Smem3(MT).total; }
+size_t wq3_gemv_smem_bytes(int MT, int S) { return Smem3(MT, S).total; }
 
 int wq3_stage_k() { return kStageK; }
 
@@ -239,7 +227,7 @@ cudaError_t launch_wq3_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const 
     default: return cudaErrorInvalidValue;
   }
   const CUtensorMap* maps[2] = {&wmap, &xmap};
-  return launch_gemv_kernel(kern, p, Smem3(p.MT).total, maps, 2, a);
+  return launch_gemv_kernel(kern, p, Smem3(p.MT, p.S).total, maps, 2, a);
 }
 
 }  // namespace wq

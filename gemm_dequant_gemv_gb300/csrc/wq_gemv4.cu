@@ -32,9 +32,9 @@ __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(
 
 // Shared-memory carve-up (same arithmetic on host and device).
 struct Smem4 {
-  size_t xst, xc, aux, zw, xfull, part, bars, flag, total;
+  size_t xst, xc, aux, zw, xfull, recv, bars, flag, total;
   // xfull_bytes: the whole x (MT rows of K values) for the permuted variant, else 0
-  __host__ __device__ Smem4(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes = 0) {
+  __host__ __device__ Smem4(int MT, int ng_max, bool act_order, int G, int S, size_t xfull_bytes = 0) {
     size_t o = size_t(kNS) * kStageBytes;
     // raw x (or the perm slice of the sorted variant) per stage, then g_idx per stage for act-order
     xst = o;  o = align16(o + size_t(kNS) * (MT * kStageK * 2 > kStageK * 4 ? MT * kStageK * 2 : kStageK * 4));
@@ -45,8 +45,8 @@ struct Smem4 {
     else           o = align16(o + size_t(ng_max) * kBN * 2);
     zw = o;   o = align16(o + (act_order ? 0 : size_t(ng_max) * (kBN / 8) * 4));
     xfull = o; o = align16(o + xfull_bytes);
-    part = o; o = align16(o + size_t(MT) * kBN * 4);
-    bars = o; o = align16(o + size_t(2 * kNS) * 8);
+    recv = o; o = align16(o + TileReduce(S, kBN).recv_floats(MT) * 4);
+    bars = o; o = align16(o + size_t(2 * kNS + 1) * 8);
     flag = o; o = align16(o + 16);
     total = o;
   }
@@ -101,16 +101,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     k4_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Smem4 L(MT, a.ng_max, false, 0, PERM ? size_t(MT) * a.K * 2 : 0);
+  const Smem4 L(MT, a.ng_max, false, 0, gridDim.x, PERM ? size_t(MT) * a.K * 2 : 0);
+  const TileReduce R(gridDim.x, kBN);
   const uint16_t* xfull = reinterpret_cast<const uint16_t*>(smem + L.xfull);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
   uint16_t* scl = reinterpret_cast<uint16_t*>(smem + L.aux);
   uint32_t* zw = reinterpret_cast<uint32_t*>(smem + L.zw);
-  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
+  uint64_t* recv_bar = empty + kNS;
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);       // producer's
   volatile int* cfailed = failed + 1;                                            // consumers'
 
@@ -130,9 +132,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     *failed = 0;
     *cfailed = 0;
+    R.init_bar(recv_bar, MT, kBN);
     fence_mbar_init();
   }
   __syncthreads();
+  if (S > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
@@ -142,6 +146,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                                    empty, n0, 4 * u0, kStageRows, 32 * u0, kStageK, n_loads, failed);
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
+    __syncwarp();
+    if (S > 1) cluster_wait();
   } else {
     const int tid = threadIdx.x;
     // scale (and zero) slice of this CTA: weight-side data, read before the dependency wait
@@ -230,25 +236,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // cross-warp reduction (the stage ring is free: every issued load was consumed)
-    consumer_sync(kConsumerThreads);
-    float* red = reinterpret_cast<float*>(wst);
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-      *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
-          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-    consumer_sync(kConsumerThreads);
-    for (int e = tid; e < MT * kBN; e += kConsumerThreads) {
-      const int m = e / kBN, col = e % kBN;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * MT + m) * kBN + col];
-      part[e] = v;
-    }
+    push_partials<MT, kBN>(R, acc, recv, recv_bar, warp, lane);
   }
 
   uint16_t* Y = static_cast<uint16_t*>(a.y);
-  finish_tile<MT, kBN>(part, S, [&](int m, int col, float v) {
+  owner_reduce_store<MT, kBN>(R, recv, recv_bar, [&](int m, int col, float v) {
     const int n = n0 + col;
     if (m < M && n < N) Y[size_t(m) * N + n] = f32_to_act<ACT_BF16>(v);
   });
@@ -264,16 +256,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                     const __grid_constant__ CUtensorMap gmap, const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int G = a.K / a.group;
-  const Smem4 L(MT, 0, true, G);
+  const Smem4 L(MT, 0, true, G, gridDim.x);
+  const TileReduce R(gridDim.x, kBN);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
   uint8_t* gst = smem + L.xst + size_t(kNS) * (MT * kStageK * 2 > kStageK * 4 ? MT * kStageK * 2 : kStageK * 4);
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
   uint32_t* goff = reinterpret_cast<uint32_t*>(smem + L.aux);        // [256] byte offsets of sd rows
   uint8_t* sd = smem + L.aux + size_t(kStageK) * 4;                  // [G][2 halves][32 lanes] x float4
-  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
+  uint64_t* recv_bar = empty + kNS;
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);       // producer's
   volatile int* cfailed = failed + 1;                                            // consumers'
 
@@ -292,9 +286,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     *failed = 0;
     *cfailed = 0;
+    R.init_bar(recv_bar, MT, kBN);
     fence_mbar_init();
   }
   __syncthreads();
+  if (S > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
@@ -329,6 +325,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
+    __syncwarp();
+    if (S > 1) cluster_wait();
   } else {
     const int tid = threadIdx.x;
     const uint16_t* SC = static_cast<const uint16_t*>(a.scales);
@@ -419,24 +417,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    consumer_sync(kConsumerThreads);
-    float* red = reinterpret_cast<float*>(wst);
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-      *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
-          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-    consumer_sync(kConsumerThreads);
-    for (int e = tid; e < MT * kBN; e += kConsumerThreads) {
-      const int m = e / kBN, col = e % kBN;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * MT + m) * kBN + col];
-      part[e] = v;
-    }
+    push_partials<MT, kBN>(R, acc, recv, recv_bar, warp, lane);
   }
 
   uint16_t* Y = static_cast<uint16_t*>(a.y);
-  finish_tile<MT, kBN>(part, S, [&](int m, int col, float v) {
+  owner_reduce_store<MT, kBN>(R, recv, recv_bar, [&](int m, int col, float v) {
     const int n = n0 + col;
     if (m < M && n < N) Y[size_t(m) * N + n] = f32_to_act<ACT_BF16>(v);
   });
@@ -454,12 +439,12 @@ cudaError_t launch_one(const LaunchPlan& p, const CUtensorMap& w, const CUtensor
                        const GemvArgs& a, int mode) {
   if (mode == 1)
     return launch3(reinterpret_cast<const void*>(k4g_gemv_kernel<MT, ACT, HZ>), p,
-                   Smem4(MT, a.ng_max, true, a.K / a.group).total, w, x, g, a);
+                   Smem4(MT, a.ng_max, true, a.K / a.group, p.S).total, w, x, g, a);
   if (mode == 2)
     return launch3(reinterpret_cast<const void*>(k4_gemv_kernel<MT, ACT, HZ, true>), p,
-                   Smem4(MT, a.ng_max, false, 0, size_t(MT) * a.K * 2).total, w, x, nullptr, a);
+                   Smem4(MT, a.ng_max, false, 0, p.S, size_t(MT) * a.K * 2).total, w, x, nullptr, a);
   return launch3(reinterpret_cast<const void*>(k4_gemv_kernel<MT, ACT, HZ, false>), p,
-                 Smem4(MT, a.ng_max, false, 0).total, w, x, nullptr, a);
+                 Smem4(MT, a.ng_max, false, 0, p.S).total, w, x, nullptr, a);
 }
 
 template <int MT>
@@ -471,8 +456,8 @@ cudaError_t dispatch_act(const LaunchPlan& p, const CUtensorMap& w, const CUtens
 
 }  // namespace
 
-size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes) {
-  return Smem4(MT, ng_max, act_order, G, xfull_bytes).total;
+size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, int S, size_t xfull_bytes) {
+  return Smem4(MT, ng_max, act_order, G, S, xfull_bytes).total;
 }
 
 int wq4_stage_k() { return kStageK; }

@@ -26,14 +26,14 @@ constexpr int kNS = 4;
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct Smem8 {
-  size_t xst, xc, scl, part, bars, flag, total;
-  __host__ __device__ Smem8(int MT, int ng_max) {
+  size_t xst, xc, scl, recv, bars, flag, total;
+  __host__ __device__ Smem8(int MT, int ng_max, int S) {
     size_t o = size_t(kNS) * kStageBytes;
     xst = o;  o = align16(o + size_t(kNS) * MT * kStageK * 4);
     xc = o;   o = align16(o + size_t(MT) * kStageK * 8);
     scl = o;  o = align16(o + size_t(ng_max) * kBN * 4);
-    part = o; o = align16(o + size_t(MT) * kBN * 4);
-    bars = o; o = align16(o + size_t(2 * kNS) * 8);
+    recv = o; o = align16(o + TileReduce(S, kBN).recv_floats(MT) * 4);
+    bars = o; o = align16(o + size_t(2 * kNS + 1) * 8);
     flag = o; o = align16(o + 16);
     total = o;
   }
@@ -44,14 +44,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     k8_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Smem8 L(MT, a.ng_max);
+  const Smem8 L(MT, a.ng_max, gridDim.x);
+  const TileReduce R(gridDim.x, kBN);
   uint8_t* wst = smem;
   uint8_t* xst = smem + L.xst;
   float2* xc = reinterpret_cast<float2*>(smem + L.xc);
   float* scl = reinterpret_cast<float*>(smem + L.scl);
-  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
+  uint64_t* recv_bar = empty + kNS;
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);  // producer's
   volatile int* cfailed = failed + 1;                                       // consumers'
 
@@ -72,9 +74,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     *failed = 0;
     *cfailed = 0;
+    R.init_bar(recv_bar, MT, kBN);
     fence_mbar_init();
   }
   __syncthreads();
+  if (S > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
@@ -84,6 +88,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                                    kStageRows, kUnitRows * u0, kStageK, n_loads, failed);
     pdl_wait();
     if (lane == 0 && *failed) drain_stages<kNS>(full, issued);
+    __syncwarp();
+    if (S > 1) cluster_wait();
   } else {
     const int tid = threadIdx.x;
     const float* SC = static_cast<const float*>(a.scales);
@@ -157,24 +163,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    consumer_sync(kConsumerThreads);
-    float* red = reinterpret_cast<float*>(wst);  // [8 warps][MT][BN] = 4 KB * MT <= 64 KB
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-      *reinterpret_cast<float4*>(red + (warp * MT + m) * kBN + lane * 4) =
-          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-    consumer_sync(kConsumerThreads);
-    for (int e = tid; e < MT * kBN; e += kConsumerThreads) {
-      const int m = e / kBN, col = e % kBN;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * MT + m) * kBN + col];
-      part[e] = v;
-    }
+    push_partials<MT, kBN>(R, acc, recv, recv_bar, warp, lane);
   }
 
   float* Y = static_cast<float*>(a.y);
-  finish_tile<MT, kBN>(part, S, [&](int m, int col, float v) {
+  owner_reduce_store<MT, kBN>(R, recv, recv_bar, [&](int m, int col, float v) {
     const int n = n0 + col;
     if (m < M && n < N) Y[size_t(m) * N + n] = v;
   });
@@ -182,7 +175,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
 }  // namespace
 
-size_t wq8_gemv_smem_bytes(int MT, int ng_max) { return Smem8(MT, ng_max).total; }
+size_t wq8_gemv_smem_bytes(int MT, int ng_max, int S) { return Smem8(MT, ng_max, S).total; }
 
 int wq8_stage_k() { return kStageK; }
 
@@ -197,7 +190,7 @@ cudaError_t launch_wq8_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const 
     default: return cudaErrorInvalidValue;
   }
   const CUtensorMap* maps[2] = {&wmap, &xmap};
-  return launch_gemv_kernel(kern, p, Smem8(p.MT, a.ng_max).total, maps, 2, a);
+  return launch_gemv_kernel(kern, p, Smem8(p.MT, a.ng_max, p.S).total, maps, 2, a);
 }
 
 }  // namespace wq

@@ -9,10 +9,11 @@
 //     of packed weight rows and the matching box of x (all M rows) into a ring
 //     of NS shared-memory stages with 2D TMA loads, gated by full/empty
 //     mbarriers.  Weights are requested before griddepcontrol.wait, x after;
-//   * warps 0..7 are consumers: per stage they first convert the stage's x
-//     block cooperatively (one named barrier), then each takes one "unit" (a
-//     fixed number of packed rows), unpacks the codes in registers, converts
-//     them with exact bit tricks and accumulates in fp32 with packed FFMA2.
+//   * warps 0..7 are consumers: per stage each converts its own slice of the
+//     stage's x, takes one "unit" (a fixed number of packed rows), unpacks
+//     the codes in registers, converts them with exact bit tricks and
+//     accumulates in fp32 with packed FFMA2.  Warps run independently; only
+//     the stage mbarriers order them.
 #pragma once
 
 #include "wq_device.cuh"
@@ -90,13 +91,90 @@ __device__ __forceinline__ void drain_stages(uint64_t* full, int issued) {
   }
 }
 
-// Final reduction of the S partial tiles of a cluster and the store of y.
-// `part` is this CTA's [MT][BN] fp32 partial in shared memory, written by the
-// consumer warps.  Every thread of the CTA must call this (it contains CTA-
-// and cluster-wide barriers).  The S CTAs of a cluster each reduce one
-// contiguous chunk of the tile, reading the other CTAs' partials through
-// distributed shared memory in rank order (a fixed summation order: the
-// result does not depend on timing).  store(m, col, value) writes one output.
+// Cross-warp / cross-CTA reduction without CTA-wide barriers.
+//
+// The tile's BN columns are split into S column chunks of `chunk` columns
+// (a multiple of 4), chunk r owned by cluster rank r.  When a consumer warp
+// has finished its K-slice, each lane sends its 4 columns (one 16-byte
+// asynchronous remote store per row m) into slot (sender rank, warp) of the
+// owner's receive buffer; the stores are counted on the owner's `recv_bar`,
+// which was primed at start for all S * 8 pieces.  Each CTA then waits on its
+// own recv_bar and adds, for its own columns, the S * 8 pieces in a fixed
+// (rank, warp) order -- the result does not depend on timing -- and stores y.
+// A cluster barrier (arrive at start, wait before the first remote store)
+// makes sure every CTA's recv_bar is initialized before anything reaches it.
+// Without a cluster (S == 1) the pieces are plain shared-memory stores and
+// recv_bar counts one arrival per consumer thread instead of bytes.
+struct TileReduce {
+  int S, chunk;  // columns per owner (multiple of 4)
+  __host__ __device__ TileReduce(int S_, int BN) : S(S_), chunk(((BN + S_ - 1) / S_ + 3) & ~3) {}
+  __host__ __device__ int piece(int MT) const { return MT * chunk; }  // floats per (sender warp, owner)
+  __host__ __device__ size_t recv_floats(int MT) const { return size_t(S) * kConsumerWarps * piece(MT); }
+  // bytes one owner receives: S CTAs x 8 warps, MT rows of its columns
+  __host__ __device__ uint32_t recv_bytes(int MT, int BN, int owner) const {
+    const int len = min(chunk, BN - owner * chunk);
+    return len > 0 ? uint32_t(S) * kConsumerWarps * MT * len * 4u : 0u;
+  }
+  // One thread, before the CTA's first cluster barrier arrive.
+  __device__ void init_bar(uint64_t* recv_bar, int MT, int BN) const {
+    if (S == 1) {
+      mbar_init(recv_bar, kConsumerThreads);
+      return;
+    }
+    mbar_init(recv_bar, 1);
+    const uint32_t rb = recv_bytes(MT, BN, cluster_rank());
+    if (rb) mbar_expect_tx(recv_bar, rb);
+  }
+};
+
+// Consumer warp: send this warp's partial sums (columns 4*lane .. 4*lane+3 of
+// the tile, MT rows) to their owner.  Waits first for the cluster barrier the
+// CTA arrived on after initialising recv_bar.
+template <int MT, int BN>
+__device__ __forceinline__ void push_partials(const TileReduce& R, const float2 (*acc)[2], float* recv,
+                                              uint64_t* recv_bar, int warp, int lane) {
+  static_assert(BN == 128, "one column quad per lane");
+  const int col = 4 * lane, r = col / R.chunk, cc = col % R.chunk;
+  if (R.S == 1) {
+    float* slot = recv + size_t(warp) * R.piece(MT);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      *reinterpret_cast<float4*>(slot + m * R.chunk + cc) =
+          make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+    mbar_arrive(recv_bar);  // release: the stores above are visible to the waiter
+    return;
+  }
+  __syncwarp();
+  cluster_wait();
+  const uint32_t me = cluster_rank();
+  float* slot = recv + (size_t(me) * kConsumerWarps + warp) * R.piece(MT);
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+    st_async_v4_to_rank(smem_u32(slot + m * R.chunk + cc), acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y,
+                        smem_u32(recv_bar), uint32_t(r));
+}
+
+// Every thread of the CTA: wait for this CTA's pieces and store its columns.
+template <int MT, int BN, class StoreFn>
+__device__ __forceinline__ void owner_reduce_store(const TileReduce& R, const float* recv, uint64_t* recv_bar,
+                                                   StoreFn store) {
+  const uint32_t me = R.S > 1 ? cluster_rank() : 0u;
+  const int c0 = int(me) * R.chunk;
+  const int len = min(R.chunk, BN - c0);
+  if (len <= 0) return;
+  if (!mbar_wait(recv_bar, 0)) return;
+  const int n_pieces = R.S * kConsumerWarps;
+  for (int e = threadIdx.x; e < MT * len; e += blockDim.x) {
+    const int m = e / len, cc = e % len;
+    float v = 0.f;
+    for (int p = 0; p < n_pieces; ++p) v += recv[size_t(p) * R.piece(MT) + m * R.chunk + cc];
+    store(m, c0 + cc, v);
+  }
+}
+
+// CTA-level reduction used by the tensor-core kernel: `part` holds this CTA's
+// MT x BN partial tile; the S CTAs of the cluster each add up an equal share
+// of the tile through distributed shared memory and store it.
 template <int MT, int BN, class StoreFn>
 __device__ __forceinline__ void finish_tile(const float* part, int S, StoreFn store) {
   constexpr int total = MT * BN;
@@ -106,8 +184,7 @@ __device__ __forceinline__ void finish_tile(const float* part, int S, StoreFn st
     return;
   }
   cluster_sync();
-  uint32_t rank;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const uint32_t rank = cluster_rank();
   const int chunk = (total + S - 1) / S;
   const int e0 = static_cast<int>(rank) * chunk;
   const int e1 = min(total, e0 + chunk);
@@ -117,7 +194,7 @@ __device__ __forceinline__ void finish_tile(const float* part, int S, StoreFn st
     for (int q = 0; q < S; ++q) v += ld_dsmem_f32(map_smem_to_rank(base + 4u * static_cast<uint32_t>(e), q));
     store(e / BN, e % BN, v);
   }
-  cluster_sync();
+  cluster_sync();  // keep this CTA's part alive until every peer has read it
 }
 
 }  // namespace wq

@@ -26,9 +26,9 @@ struct LaunchPlan {
 cudaError_t launch_gemv_kernel(const void* kern, const LaunchPlan& p, size_t smem_bytes,
                                const CUtensorMap* const* maps, int nmaps, const GemvArgs& a);
 
-size_t wq8_gemv_smem_bytes(int MT, int ng_max);
-size_t wq3_gemv_smem_bytes(int MT);
-size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, size_t xfull_bytes = 0);
+size_t wq8_gemv_smem_bytes(int MT, int ng_max, int S);
+size_t wq3_gemv_smem_bytes(int MT, int S);
+size_t wq4_gemv_smem_bytes(int MT, int ng_max, bool act_order, int G, int S, size_t xfull_bytes = 0);
 
 // Values of k one pipeline stage covers (the x box width of each kernel).
 int wq8_stage_k();
