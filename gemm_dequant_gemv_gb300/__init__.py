@@ -34,6 +34,8 @@ SIGNATURES = {
     "wq4_gemm_sorted": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _U, _P]),
     "w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _U, _P]),
     "w8a8_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P]),
+    "w8a8_gemm_noalloc_max_scratch_bytes": (_SZ, []),
 }
 
 
@@ -136,3 +138,14 @@ def w8a8_gemm(X, W, Sw, Y, M, K, N, Xq_out=None, Sx_out=None, acc_out=None, work
     _check("w8a8_gemm", _lib.w8a8_gemm(_ptr(X), _ptr(W), _ptr(Sw), _ptr(Y), M, K, N, _ptr(Xq_out),
                                        _ptr(Sx_out), _ptr(acc_out), _ptr(workspace), workspace_bytes,
                                        flags, _stream(stream)))
+
+
+def w8a8_gemm_noalloc_max_scratch_bytes() -> int:
+    return int(_lib.w8a8_gemm_noalloc_max_scratch_bytes())
+
+
+def w8a8_gemm_noalloc(X, W, Sw, Y, M, K, N, Xq_out=None, Sx_out=None, acc_out=None, flags=0, stream=None):
+    """w8a8_gemm on the library's built-in scratch: allocates nothing.  All calls
+    on one device share that scratch, so calls that can overlap race."""
+    _check("w8a8_gemm_noalloc", _lib.w8a8_gemm_noalloc(_ptr(X), _ptr(W), _ptr(Sw), _ptr(Y), M, K, N, _ptr(Xq_out),
+                                                       _ptr(Sx_out), _ptr(acc_out), flags, _stream(stream)))

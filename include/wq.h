@@ -203,6 +203,42 @@ WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void
 /* Bytes of device workspace w8a8_gemm needs for this shape (0 on bad shape). */
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
 
+/*
+ * w8a8_gemm_noalloc -- w8a8_gemm without a caller workspace.  The pages have
+ * no counterpart: this is library plumbing, not part of the method.
+ *
+ * Who it is for: callers that cannot allocate device memory for the
+ *   workspace -- code whose device memory is owned by someone else (a host
+ *   framework or server that reserves all of it up front), code with a fixed
+ *   memory budget, and code that must not pay for cudaMalloc / cudaFree, which
+ *   can block and (cudaFree) synchronize the whole device.  This entry point
+ *   allocates nothing: it runs w8a8_gemm on a scratch array built into the
+ *   library, one copy per device, of w8a8_gemm_noalloc_max_scratch_bytes()
+ *   bytes (8 MiB).
+ * Arguments, layouts, results and checks: as w8a8_gemm, without `workspace`.
+ * Size limit: the shape's w8a8_gemm_workspace_bytes(M, K, N) must not exceed
+ *   the built-in size (about M*K <= 4.19 million, e.g. M = 512 at K = 8192);
+ *   a larger shape returns WQ_ERR_WORKSPACE before anything runs -- use
+ *   w8a8_gemm with a workspace of your own for it.
+ * First call on each device: looks up the device address of the built-in
+ *   scratch (the CUDA runtime may load the library's device code then) and
+ *   caches it.  This set-up is done with the caller's current device, once
+ *   per device; make the first call on each device before any stream
+ *   capture begins.  A failed look-up returns WQ_ERR_CUDA.
+ * Zero state: nothing needs to start at zero; every call writes each scratch
+ *   byte it later reads.
+ * Concurrency: all calls on one device share the one scratch array.  Calls
+ *   whose executions can overlap -- on different streams without an ordering
+ *   between them, from any thread -- race on it and may return wrong
+ *   results.  Calls issued on one stream (or otherwise ordered) are safe.
+ */
+WQ_API wq_status w8a8_gemm_noalloc(const void* X, const int8_t* W, const float* Sw, void* Y,
+                                   int M, int K, int N, int8_t* Xq_out, float* Sx_out,
+                                   int32_t* acc_out, unsigned flags, void* stream);
+
+/* Bytes of the scratch array w8a8_gemm_noalloc uses (the size limit above). */
+WQ_API size_t w8a8_gemm_noalloc_max_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif
