@@ -135,6 +135,31 @@ wq_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 
+// The tensor-core 4-bit GEMV (2 <= M <= 8, group a multiple of its 64-value unit;
+// K % group == 0 was checked by the caller).  perm != nullptr: rows sorted by group.
+// For M = 1 the CUDA-core kernels are as fast or faster on GB300 (measured:
+// 44 vs 46 us at 8192 x 28672, 10.9 vs 11.6 us for the sorted 4096 x 11008),
+// while from M = 2 on the MMA path costs the same as M = 1 and the CUDA-core
+// one grows with M.
+wq_status wq4m_launch(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                      const int32_t* perm, void* y, int M, int K, int N, int group_size, int act_bf16,
+                      unsigned flags, cudaStream_t stream) {
+  const int T = (N + 127) / 128, units = K / wq4m_unit_k();
+  LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, stream};
+  GemvArgs a{x, y, scales, qzeros, nullptr, M, K, N, group_size, 0};
+  a.ng_max = max_groups_per_slice(units, p.S, wq4m_unit_k(), group_size);
+  if (wq4m_gemv_smem_bytes(p.MT, a.ng_max, p.S, perm != nullptr, K) > static_cast<size_t>(device_max_smem()))
+    return WQ_ERR_UNSUPPORTED;
+  CUtensorMap wmap, xmap;
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ERR_CUDA;
+  if (perm ? !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_INT32, perm, K, 1, 4, wq4m_stage_k(), 1)
+           : !encode_x_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, K, M, 2, wq4m_stage_k(), p.MT))
+    return WQ_ERR_CUDA;
+  return from_cuda(launch_wq4m_gemv(p, wmap, xmap, a, act_bf16, qzeros != nullptr, perm != nullptr));
+}
+
 }  // namespace
 }  // namespace wq
 
@@ -228,6 +253,10 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
                                     static_cast<cudaStream_t>(stream)));
   }
 
+  if (!g_idx && M >= 2 && group_size % wq4m_unit_k() == 0)
+    return wq4m_launch(x, qweight, scales, qzeros, nullptr, y, M, K, N, group_size, act_bf16, flags,
+                       static_cast<cudaStream_t>(stream));
+
   const int T = (N + 127) / 128, units = K / 32;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, qzeros, g_idx, M, K, N, group_size, 0};
@@ -265,6 +294,9 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
   if (!aligned16(x) || !aligned16(qweight_sorted) || !aligned16(scales) || !aligned16(perm) || !aligned16(y) ||
       (qzeros && !aligned16(qzeros)))
     return WQ_ERR_ALIGN;
+  if (M >= 2 && group_size % wq4m_unit_k() == 0)
+    return wq4m_launch(x, qweight_sorted, scales, qzeros, perm, y, M, K, N, group_size, act_dtype == WQ_BF16, flags,
+                       static_cast<cudaStream_t>(stream));
   const int T = (N + 127) / 128, units = K / 32;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, qzeros, nullptr, M, K, N, group_size, 0};

@@ -45,4 +45,13 @@ cudaError_t launch_wq4_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const 
                             const CUtensorMap* gmap, const GemvArgs& a, int act_bf16, bool has_z,
                             bool sorted = false);
 
+// 4-bit GEMV on the warp-level tensor-core MMA (contiguous groups, or rows
+// sorted by group when perm): needs K % wq4m_unit_k() == 0 and a group size
+// that is a multiple of it; the weight map uses 32 x 32 boxes, 128-byte swizzle.
+int wq4m_unit_k();
+int wq4m_stage_k();
+size_t wq4m_gemv_smem_bytes(int MT, int ng_max, int S, bool perm, int K);
+cudaError_t launch_wq4m_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                             const GemvArgs& a, int act_bf16, bool has_z, bool perm);
+
 }  // namespace wq

@@ -87,7 +87,9 @@ def test_wq3_onehot_exact(G):
 # ------------------------------------------------------------------- 4-bit ----
 WQ4_CASES = [  # M, K, N, group, bf16, asym zeros
     (1, 256, 128, 32, False, True), (3, 512, 264, 128, True, False), (8, 1024, 520, 64, False, True),
-    (2, 2048, 1032, 128, True, True), (1, 8192, 28672, 128, True, False), (8, 8192, 28672, 128, True, False)]
+    (2, 2048, 1032, 128, True, True), (1, 8192, 28672, 128, True, False), (8, 8192, 28672, 128, True, False),
+    # K not a multiple of the 256-value stage, M between the tile sizes
+    (1, 320, 136, 64, False, True), (5, 576, 200, 64, True, True), (7, 1088, 264, 64, False, False)]
 
 
 def _make_wq4(M, K, N, g, bf16, asym, seed=4):
@@ -150,6 +152,22 @@ def test_wq4_onehot_exact(G, act_order):
         assert np.array_equal(y, oracle.round_f16(y_ref)), k
 
 
+def test_wq4_onehot_exact_multirow(G):
+    """M = 3 (tensor-core path): each row of x a different one-hot vector; y rows
+    are the dequantized weight rows, rounded once (bit for bit)."""
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq4_actorder(seed=9, M=3, K=512, N=264, group=128)
+    d["g_idx"] = None
+    x = np.zeros((3, 512), np.float16)
+    for m, k in enumerate((5, 130, 511)):
+        x[m, k] = 1.0
+    d["x"] = x
+    y = G.bits_u16(G.run_wq4(d))
+    y_ref, _ = G.oracle_wq4(d)
+    assert np.array_equal(y, oracle.round_f16(y_ref))
+
+
 # ------------------------------------------------------------ invariants ----
 
 def test_repeat_bit_identical_and_pdl(G):
@@ -206,7 +224,8 @@ def test_wq4_mma_onehot_exact(G):
 
 
 # ------------------------------------------- act-order on group-sorted rows ----
-WQ4S_CASES = [(1, 256, 128, 32), (1, 4096, 11008, 128), (3, 2048, 1032, 64), (8, 1024, 256, 128)]
+WQ4S_CASES = [(1, 256, 128, 32), (1, 4096, 11008, 128), (3, 2048, 1032, 64), (8, 1024, 256, 128),
+              (5, 704, 136, 64), (2, 4096, 11008, 128)]
 
 
 @pytest.mark.parametrize("M,K,N,g", WQ4S_CASES)
