@@ -43,6 +43,10 @@ LAYERS = 16
 WORKLOAD = ("decode step through 16 layers, each: W8 g128 GEMV 4096x4096 (fp32) + W3 per-column GEMV "
             "4096x4096 (fp16) + W4 act-order g128 GEMV 4096x11008 (fp16), M=1")
 FALLBACK_HBM_GBS = 6800.0
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the roofline kernel
+# (k4_gemv_kernel, sorted rows, 4096 x 11008, M = 1), from one ncu --set full capture
+# of that kernel under this script's own command; set to None when that kernel changes.
+K4_SORTED_TRAFFIC_BYTES = 23478784
 
 
 def alg_bytes_w8(M=1, K=4096, N=4096, g=128):
@@ -541,7 +545,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "k4_gemv_kernel<1,f16,zeros,sorted> (W4 act-order GEMV 4096x11008, "
                                                "group-sorted rows)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "traffic": None},
+                     "peak_source": peak_kind, "traffic": K4_SORTED_TRAFFIC_BYTES},
         "e2e": {"value": world * res["step_bytes"] / res["e2e_s_per_step"] / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "steps": res["e2e_steps"]},
