@@ -105,9 +105,13 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
 // --------------------------------------------------------------------- GEMM --
 constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kChunkStages = 4;  // 256 values of k per exact fp32 chunk
-constexpr int kNS = 4, kNB = 2;
-constexpr int kThreads = 10 * 32;
-constexpr int kWarpTMA = 8, kWarpMMA = 9;
+constexpr int kNS = 4, kNB = 3;
+constexpr int kConvWarps = 8;            // int8 -> fp16 converters of the B tile
+constexpr int kEpiWarps = 8;             // two per tensor-memory lane quarter, 64 columns each
+constexpr int kThreads = (kConvWarps + kEpiWarps + 2) * 32;
+constexpr int kWarpTMA = kConvWarps + kEpiWarps, kWarpMMA = kWarpTMA + 1;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue thread
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB fp16 codes of X
 constexpr int kWBytes = kBK * kBN;       // 8 KB int8 W
 constexpr int kBBytes = kBN * kBK * 2;   // 16 KB fp16 W in the MN-major layout
@@ -187,12 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < kNB; ++s) {
-      mbar_init(&b_full[s], 4 * 32);
+      mbar_init(&b_full[s], kConvWarps * 32);
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&t_full[s], 1);
-      mbar_init(&t_empty[s], 4 * 32);
+      mbar_init(&t_empty[s], kEpiThreads);
     }
     *failed = 0;
     fence_mbar_init();
@@ -259,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (last >= 0) mbar_wait(&empty[last % kNS], (last / kNS) & 1);
     }
-  } else if (warp < 4) {
+  } else if (warp < kConvWarps) {
     // ---------------------------------------------------------- converters --
-    const int t = threadIdx.x;  // 0..127
+    const int t = threadIdx.x;  // 0 .. kConvWarps * 32 - 1
     for (int i = 0; i < nst; ++i) {
       const int s = i % kNS, bb = i % kNB;
       if (!mbar_wait(&full[s], (i / kNS) & 1)) { *failed = 1; break; }
@@ -269,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* wt = sW + size_t(s) * kWBytes;
       uint8_t* bt = sB + size_t(bb) * kBBytes;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int q = t + 128 * p;            // 16-byte chunk of the int8 tile: row k, columns 16c..16c+15
+      for (int p = 0; p < (kWBytes / 16) / (kConvWarps * 32); ++p) {
+        const int q = t + kConvWarps * 32 * p;  // 16-byte chunk of the int8 tile: row k, columns 16c..16c+15
         const int k = q >> 3, c = q & 7;
         const uint4 v = *reinterpret_cast<const uint4*>(wt + k * kBN + c * 16);
         const uint32_t w4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
@@ -298,25 +302,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
   } else {
     // ------------------------------------------------------------ epilogue --
+    // warp e (0..7): tensor-memory lane quarter e % 4 = tile rows 32 (e % 4) ..,
+    // columns kEpiCols * (e / 4) ..
     pdl_wait();
-    const int row = threadIdx.x - 4 * 32;  // 0..127 == tensor-memory lane == output row in the tile
-    for (int c = row; c < kBN; c += 128) sSw[c] = (n0 + c < N) ? a.Sw[n0 + c] : 0.f;
-    sSx[row] = (m0 + row < M) ? a.Sx[m0 + row] : 0.f;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    uint32_t acc[kBN];
+    const int et = threadIdx.x - kConvWarps * 32;  // 0 .. kEpiThreads - 1
+    const int ew = warp - kConvWarps, quarter = ew & 3, half = ew >> 2;
+    const int row = quarter * 32 + lane;            // tensor-memory lane == output row in the tile
+    const int cbase = half * kEpiCols;
+    for (int c = et; c < kBN; c += kEpiThreads) sSw[c] = (n0 + c < N) ? a.Sw[n0 + c] : 0.f;
+    if (half == 0) sSx[row] = (m0 + row < M) ? a.Sx[m0 + row] : 0.f;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cbase;
+    uint32_t acc[kEpiCols];
 #pragma unroll
-    for (int c = 0; c < kBN; ++c) acc[c] = 0u;
+    for (int c = 0; c < kEpiCols; ++c) acc[c] = 0u;
     int drained = 0;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int tb = ch & 1;
       if (!mbar_wait(&t_full[tb], (ch / 2) & 1)) { *failed = 1; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        float v[32];
-        tmem_ld32(lane_addr + tb * kBN + c0, v);
+      for (int c0 = 0; c0 < kEpiCols; c0 += 16) {
+        float v[16];
+        tmem_ld16(lane_addr + tb * kBN + c0, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[c0 + j] += __float_as_uint(v[j] + 12582912.0f);
+        for (int j = 0; j < 16; ++j) acc[c0 + j] += __float_as_uint(v[j] + 12582912.0f);
       }
       tc_fence_before();
       mbar_arrive(&t_empty[tb]);
@@ -324,18 +333,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t bias = uint32_t(drained) * 0x4B400000u;
     // Y = bf16(Sx * acc * Sw) staged in shared memory (the X stages are free now)
-    asm volatile("bar.sync 2, 128;" ::: "memory");  // epilogue warps: sSw / sSx complete
+    asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // epilogue warps: sSw / sSx complete
     const float sx = sSx[row];
-    uint8_t* orow = sA + size_t(row) * kOutStride;
+    uint8_t* orow = sA + size_t(row) * kOutStride + cbase * 2;
 #pragma unroll
-    for (int c0 = 0; c0 < kBN; c0 += 8) {
+    for (int c0 = 0; c0 < kEpiCols; c0 += 8) {
       uint32_t pk[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int32_t i0 = static_cast<int32_t>(acc[c0 + 2 * j] - bias);
         const int32_t i1 = static_cast<int32_t>(acc[c0 + 2 * j + 1] - bias);
-        const float f0 = (sx * static_cast<float>(i0)) * sSw[c0 + 2 * j];
-        const float f1 = (sx * static_cast<float>(i1)) * sSw[c0 + 2 * j + 1];
+        const float f0 = (sx * static_cast<float>(i0)) * sSw[cbase + c0 + 2 * j];
+        const float f1 = (sx * static_cast<float>(i1)) * sSw[cbase + c0 + 2 * j + 1];
         pk[j] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f0))) |
                 (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f1))) << 16);
       }
@@ -343,14 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.acc_out && m0 + row < M) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (n0 + c0 + j < N)
-            a.acc_out[size_t(m0 + row) * N + n0 + c0 + j] = static_cast<int32_t>(acc[c0 + j] - bias);
+          if (n0 + cbase + c0 + j < N)
+            a.acc_out[size_t(m0 + row) * N + n0 + cbase + c0 + j] = static_cast<int32_t>(acc[c0 + j] - bias);
       }
     }
-    asm volatile("bar.sync 2, 128;" ::: "memory");
+    asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
     // coalesced stores: 16 chunks of 16 bytes per tile row
     uint16_t* Y = static_cast<uint16_t*>(a.Y);
-    for (int q = row; q < kBM * (kBN / 8); q += 128) {
+    for (int q = et; q < kBM * (kBN / 8); q += kEpiThreads) {
       const int r = q / (kBN / 8), c = (q % (kBN / 8)) * 8;
       if (m0 + r < M && n0 + c < N)
         *reinterpret_cast<uint4*>(Y + size_t(m0 + r) * N + n0 + c) = *reinterpret_cast<const uint4*>(sA + size_t(r) * kOutStride + c * 2);

@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   int u0, u1;
   split_range(K / 32, S, blockIdx.x, u0, u1);
   const int n_loads = (u1 - u0 + kConsumerWarps - 1) / kConsumerWarps;
-  const int g0 = (32 * u0) / gsz;
+  const UnitGroups ug(gsz, 32);
+  const int g0 = ug.of(u0);
   const int ng = (u1 > u0) ? (32 * u1 - 1) / gsz - g0 + 1 : 0;
 
   if (threadIdx.x == 0) {
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         for (int i = 0; i < kUnitRows; ++i)
           unit_row_accumulate<MT>(*reinterpret_cast<const uint4*>(rowp + i * (kBN * 4)), xw + 4 * i, accg);
         // apply the unit's group scale, removing the 128 x offset and the zero point
-        const int gi = (32 * u) / gsz - g0;
+        const int gi = ug.of(u) - g0;
         const uint2 sv = *reinterpret_cast<const uint2*>(scl + gi * kBN + lane * 4);
         const float2 s01 = make_float2(scale_bits_to_f32<ACT_BF16>(sv.x & 0xFFFFu), scale_bits_to_f32<ACT_BF16>(sv.x >> 16));
         const float2 s23 = make_float2(scale_bits_to_f32<ACT_BF16>(sv.y & 0xFFFFu), scale_bits_to_f32<ACT_BF16>(sv.y >> 16));

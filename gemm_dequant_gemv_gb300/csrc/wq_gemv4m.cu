@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   int u0, u1;
   split_range(K / kUnitK, S, blockIdx.x, u0, u1);
   const int n_loads = (u1 - u0 + kUnitsPerStage - 1) / kUnitsPerStage;
-  const int g0 = (kUnitK * u0) / gsz;
+  const UnitGroups ug(gsz, kUnitK);
+  const int g0 = ug.of(u0);
   const int ng = (u1 > u0) ? (kUnitK * u1 - 1) / gsz - g0 + 1 : 0;
   constexpr uint32_t kXBytes = PERM ? kStageK * 4 : MT * kStageK * 2;
 
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       for (int j = 0; j < 2; ++j) {
         const int u = u0 + kUnitsPerStage * it + 2 * khalf + j;
         if (u >= u1) break;
-        const int gi = (kUnitK * u) / gsz - g0;
+        const int gi = ug.of(u) - g0;
         if (gi != cur_g) {  // a new scale group: apply the finished one, load the new zeros
           if (cur_g >= 0) fold(cur_g);
           cur_g = gi;

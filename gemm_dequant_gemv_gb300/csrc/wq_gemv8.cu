@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   int u0, u1;
   split_range(K / kUnitRows, S, blockIdx.x, u0, u1);
   const int n_loads = (u1 - u0 + kConsumerWarps - 1) / kConsumerWarps;
-  const int g0 = (kUnitRows * u0) / gsz;
+  const UnitGroups ug(gsz, kUnitRows);
+  const int g0 = ug.of(u0);
   const int ng = (u1 > u0) ? (kUnitRows * u1 - 1) / gsz - g0 + 1 : 0;
   constexpr uint32_t kXBytes = MT * kStageK * 4;
 
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             }
           }
         }
-        const int gi = (kUnitRows * u) / gsz - g0;
+        const int gi = ug.of(u) - g0;
         const float4 sv = *reinterpret_cast<const float4*>(scl + gi * kBN + lane * 4);
         const float2 s01 = make_float2(sv.x, sv.y), s23 = make_float2(sv.z, sv.w);
 #pragma unroll

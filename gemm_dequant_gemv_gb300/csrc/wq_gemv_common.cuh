@@ -40,6 +40,17 @@ __device__ __forceinline__ void split_range(int units, int S, int s, int& u0, in
   u1 = static_cast<int>((static_cast<long long>(s + 1) * units) / S);
 }
 
+// Group index of work unit u (units of `unit_k` values of k, groups of `group`
+// values, group a multiple of unit_k): a shift when the number of units per
+// group is a power of two (the usual 64, 128, 256), a division otherwise.
+struct UnitGroups {
+  int per, shift;  // units per group; log2(per) or -1
+  __device__ UnitGroups(int group, int unit_k) : per(group / unit_k) {
+    shift = (per & (per - 1)) == 0 ? __ffs(per) - 1 : -1;
+  }
+  __device__ __forceinline__ int of(int u) const { return shift >= 0 ? (u >> shift) : u / per; }
+};
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
