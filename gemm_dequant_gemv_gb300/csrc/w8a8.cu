@@ -103,21 +103,23 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
 }
 
 // --------------------------------------------------------------------- GEMM --
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kChunkStages = 4;  // 256 values of k per exact fp32 chunk
-constexpr int kNS = 4, kNB = 3;
+constexpr int kBM = 128, kBN = 128, kBK = 128;
+constexpr int kBoxK = 64;                    // values of k per 128-byte-swizzled X box
+constexpr int kChunkStages = 256 / kBK;      // 256 values of k per exact fp32 chunk
+constexpr int kNS = 3, kNB = 2;
 constexpr int kConvWarps = 8;            // int8 -> fp16 converters of the B tile
 constexpr int kEpiWarps = 8;             // two per tensor-memory lane quarter, 64 columns each
 constexpr int kThreads = (kConvWarps + kEpiWarps + 2) * 32;
 constexpr int kWarpTMA = kConvWarps + kEpiWarps, kWarpMMA = kWarpTMA + 1;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue thread
-constexpr int kABytes = kBM * kBK * 2;   // 16 KB fp16 codes of X
-constexpr int kWBytes = kBK * kBN;       // 8 KB int8 W
-constexpr int kBBytes = kBN * kBK * 2;   // 16 KB fp16 W in the MN-major layout
+constexpr int kABoxBytes = kBM * kBoxK * 2;  // 16 KB: one X box (128 rows x 64 k)
+constexpr int kABytes = kBM * kBK * 2;       // 32 KB fp16 codes of X per stage (two boxes)
+constexpr int kWBytes = kBK * kBN;           // 16 KB int8 W
+constexpr int kBBytes = kBN * kBK * 2;       // 32 KB fp16 W in the MN-major layout
 // MN-major 128-byte-swizzle atoms of the B operand: 8 rows of k x 64 values of n.
-constexpr uint32_t kAtomK = 1024;        // byte stride between k-atoms (adjacent)
-constexpr uint32_t kAtomN = 8 * 1024;    // byte stride between the two n-atoms
+constexpr uint32_t kAtomK = 1024;                      // byte stride between k-atoms (adjacent)
+constexpr uint32_t kAtomN = (kBK / 8) * kAtomK;        // byte stride between the two n-atoms
 constexpr int kOutStride = kBN * 2 + 16; // padded bf16 output row in shared memory
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
   const int M = a.M, K = a.K, N = a.N;
-  const int nst = K / kBK;
+  const int nst = (K + kBK - 1) / kBK;  // the tail of the last stage is zero-filled by TMA
   const int nchunks = (nst + kChunkStages - 1) / kChunkStages;
   constexpr uint32_t kTmemCols = 2 * kBN;
 
@@ -219,7 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sW + size_t(i) * kWBytes, &wmap, &full[i], n0, i * kBK, 0ull);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) tma_load_2d(sA + size_t(i) * kABytes, &amap, &full[i], i * kBK, m0, 0ull);
+      for (int i = 0; i < pre; ++i)
+#pragma unroll
+        for (int h = 0; h < kBK / kBoxK; ++h)
+          tma_load_2d(sA + size_t(i) * kABytes + h * kABoxBytes, &amap, &full[i], i * kBK + h * kBoxK, m0, 0ull);
       for (int i = kNS; i < nst && !*failed; ++i) {
         const int s = i % kNS;
         if (!mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
@@ -228,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_expect_tx(&full[s], kABytes + kWBytes);
         tma_load_2d(sW + size_t(s) * kWBytes, &wmap, &full[s], n0, i * kBK, 0ull);
-        tma_load_2d(sA + size_t(s) * kABytes, &amap, &full[s], i * kBK, m0, 0ull);
+#pragma unroll
+        for (int h = 0; h < kBK / kBoxK; ++h)
+          tma_load_2d(sA + size_t(s) * kABytes + h * kABoxBytes, &amap, &full[s], i * kBK + h * kBoxK, m0, 0ull);
       }
     } else {
       pdl_wait();
@@ -254,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_base = smem_u32(sB + size_t(bb) * kBBytes);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          mma_f16(tmem + tb * kBN, sw128_kmajor_desc(a_base + 32 * k), sw128_mnmajor_desc(b_base + 2 * kAtomK * k),
+          mma_f16(tmem + tb * kBN, sw128_kmajor_desc(a_base + (k / (kBoxK / 16)) * kABoxBytes + 32 * (k % (kBoxK / 16))),
+                  sw128_mnmajor_desc(b_base + 2 * kAtomK * k),
                   idesc, (i % kChunkStages != 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
         mma_commit(&b_empty[bb]);
@@ -274,8 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* bt = sB + size_t(bb) * kBBytes;
 #pragma unroll
       for (int p = 0; p < (kWBytes / 16) / (kConvWarps * 32); ++p) {
-        const int q = t + kConvWarps * 32 * p;  // 16-byte chunk of the int8 tile: row k, columns 16c..16c+15
-        const int k = q >> 3, c = q & 7;
+        // 16-byte chunk (row k, columns 16c..16c+15) of the int8 tile.  Within each
+        // 8-lane phase k % 8 = i runs over 0..7 and c = (i + d) % 8, so that the
+        // loads (chunk c of a 128-byte row) and both swizzled stores (chunk
+        // (2 (c % 4) [+1]) ^ (k % 8)) hit 8 different bank groups.
+        const int q = t + kConvWarps * 32 * p;
+        const int i = q & 7, rest = q >> 3;
+        const int k = 8 * (rest % (kBK / 8)) + i, c = (i + rest / (kBK / 8)) & 7;
         const uint4 v = *reinterpret_cast<const uint4*>(wt + k * kBN + c * 16);
         const uint32_t w4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
         uint32_t h[8];
@@ -417,7 +430,7 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
   }
   // 2) GEMM with the fused rescale epilogue (always chained to the quantization kernel)
   CUtensorMap amap, wmap;
-  if (!encode_tensor_map_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xq16, K, M, size_t(K) * 2, kBK, kBM,
+  if (!encode_tensor_map_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xq16, K, M, size_t(K) * 2, kBoxK, kBM,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, N, K, N, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;

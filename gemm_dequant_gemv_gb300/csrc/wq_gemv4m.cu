@@ -129,6 +129,18 @@ __device__ __forceinline__ void convert_word(uint32_t w, uint32_t zsub, uint32_t
   }
 }
 
+// Code pair `pi` (0: codes 0,4; 1: 1,5; 2: 2,6; 3: 3,7) of one packed word as q - z.
+template <int ACT_BF16, int PI>
+__device__ __forceinline__ uint32_t convert_pair(uint32_t w, uint32_t zsub, uint32_t zfma) {
+  if (ACT_BF16) {
+    return hsub2_bf16(lop3_and_or(w >> (4 * PI), 0x000F000Fu, 0x43004300u), zsub);
+  } else {
+    const uint32_t ws = (PI >= 2) ? (w >> 8) : w;
+    if (PI & 1) return hfma2_f16(lop3_and_or(ws, 0x00F000F0u, 0x64006400u), 0x2C002C00u, zfma);
+    return hsub2_f16(lop3_and_or(ws, 0x000F000Fu, 0x64006400u), zsub);
+  }
+}
+
 template <int ACT_BF16>
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -362,19 +374,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 #pragma unroll
         for (int ab = 0; ab < 2; ++ab) {
           const uint32_t w4[4] = {wv[ab].x, wv[ab].y, wv[ab].z, wv[ab].w};
-          uint32_t P[4][4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) convert_word<ACT_BF16>(w4[c], zsv[c], zfv[c], P[c]);
           const uint32_t b[4] = {prmt(xv[ab].x, xv[ab].z, 0x5410u),   // (x0, x4)
                                  prmt(xv[ab].x, xv[ab].z, 0x7632u),   // (x1, x5)
                                  prmt(xv[ab].y, xv[ab].w, 0x5410u),   // (x2, x6)
                                  prmt(xv[ab].y, xv[ab].w, 0x7632u)};  // (x3, x7)
 #pragma unroll
-          for (int st = 0; st < 2; ++st) {
-            mma_16816<ACT_BF16>(tmp[ab][0], P[0][2 * st], P[1][2 * st], P[0][2 * st + 1], P[1][2 * st + 1],
-                                b[2 * st], b[2 * st + 1]);
-            mma_16816<ACT_BF16>(tmp[ab][1], P[2][2 * st], P[3][2 * st], P[2][2 * st + 1], P[3][2 * st + 1],
-                                b[2 * st], b[2 * st + 1]);
+          for (int tl = 0; tl < 2; ++tl) {
+            // operands in MMA order: rows g (word 2tl) and g+8 (word 2tl+1), low then high k slots
+            const uint32_t we = w4[2 * tl], wo = w4[2 * tl + 1];
+            const uint32_t zse = zsv[2 * tl], zso = zsv[2 * tl + 1], zfe = zfv[2 * tl], zfo = zfv[2 * tl + 1];
+            mma_16816<ACT_BF16>(tmp[ab][tl], convert_pair<ACT_BF16, 0>(we, zse, zfe), convert_pair<ACT_BF16, 0>(wo, zso, zfo),
+                                convert_pair<ACT_BF16, 1>(we, zse, zfe), convert_pair<ACT_BF16, 1>(wo, zso, zfo), b[0], b[1]);
+            mma_16816<ACT_BF16>(tmp[ab][tl], convert_pair<ACT_BF16, 2>(we, zse, zfe), convert_pair<ACT_BF16, 2>(wo, zso, zfo),
+                                convert_pair<ACT_BF16, 3>(we, zse, zfe), convert_pair<ACT_BF16, 3>(wo, zso, zfo), b[2], b[3]);
           }
         }
       }
