@@ -133,7 +133,7 @@ struct SmemW8A8 {
     w = o;    o += size_t(kNS) * kWBytes;
     sw = o;   o = align_up(o + kBN * 4, 16);
     sx = o;   o = align_up(o + kBM * 4, 16);
-    bars = o; o = align_up(o + size_t(2 * kNS + 2 * kNB + 4) * 8, 16);
+    bars = o; o = align_up(o + size_t(4 * kNS + 2 * kNB + 4) * 8, 16);
     misc = o; o = align_up(o + 32, 16);
     total = o + 1024;
   }
@@ -171,9 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sW = smem + L.w;
   float* sSw = reinterpret_cast<float*>(smem + L.sw);
   float* sSx = reinterpret_cast<float*>(smem + L.sx);
+  // full / empty: the X-code ring (released when the MMA has read a stage);
+  // wfull / wempty: the int8 W ring (released as soon as the converters have read it)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
-  uint64_t* b_full = empty + kNS;
+  uint64_t* wfull = empty + kNS;
+  uint64_t* wempty = wfull + kNS;
+  uint64_t* b_full = wempty + kNS;
   uint64_t* b_empty = b_full + kNB;
   uint64_t* t_full = b_empty + kNB;
   uint64_t* t_empty = t_full + 2;
@@ -191,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], kConvWarps * 32);
     }
     for (int s = 0; s < kNB; ++s) {
       mbar_init(&b_full[s], kConvWarps * 32);
@@ -212,27 +218,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ producer --
+    // lane 0 streams the int8 W tiles (weight-side data: no dependency wait, the
+    // converters can start before the previous kernel has finished); lane 1
+    // streams the fp16 X codes after the wait.
     if (lane == 0) {
-      prefetch_tensormap(&amap);
       prefetch_tensormap(&wmap);
-      const int pre = nst < kNS ? nst : kNS;
-      for (int i = 0; i < pre; ++i) {  // weights before the dependency wait, the X codes after it
-        mbar_expect_tx(&full[i], kABytes + kWBytes);
-        tma_load_2d(sW + size_t(i) * kWBytes, &wmap, &full[i], n0, i * kBK, 0ull);
-      }
-      pdl_wait();
-      for (int i = 0; i < pre; ++i)
-#pragma unroll
-        for (int h = 0; h < kBK / kBoxK; ++h)
-          tma_load_2d(sA + size_t(i) * kABytes + h * kABoxBytes, &amap, &full[i], i * kBK + h * kBoxK, m0, 0ull);
-      for (int i = kNS; i < nst && !*failed; ++i) {
+      for (int i = 0; i < nst && !*failed; ++i) {
         const int s = i % kNS;
-        if (!mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
+        if (i >= kNS && !mbar_wait(&wempty[s], ((i / kNS) - 1) & 1)) {
           *failed = 1;
           break;
         }
-        mbar_expect_tx(&full[s], kABytes + kWBytes);
-        tma_load_2d(sW + size_t(s) * kWBytes, &wmap, &full[s], n0, i * kBK, 0ull);
+        mbar_expect_tx(&wfull[s], kWBytes);
+        tma_load_2d(sW + size_t(s) * kWBytes, &wmap, &wfull[s], n0, i * kBK, 0ull);
+      }
+    } else if (lane == 1) {
+      prefetch_tensormap(&amap);
+      pdl_wait();
+      for (int i = 0; i < nst && !*failed; ++i) {
+        const int s = i % kNS;
+        if (i >= kNS && !mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
+          *failed = 1;
+          break;
+        }
+        mbar_expect_tx(&full[s], kABytes);
 #pragma unroll
         for (int h = 0; h < kBK / kBoxK; ++h)
           tma_load_2d(sA + size_t(s) * kABytes + h * kABoxBytes, &amap, &full[s], i * kBK + h * kBoxK, m0, 0ull);
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = threadIdx.x;  // 0 .. kConvWarps * 32 - 1
     for (int i = 0; i < nst; ++i) {
       const int s = i % kNS, bb = i % kNB;
-      if (!mbar_wait(&full[s], (i / kNS) & 1)) { *failed = 1; break; }
+      if (!mbar_wait(&wfull[s], (i / kNS) & 1)) { *failed = 1; break; }
       if (i >= kNB && !mbar_wait(&b_empty[bb], ((i / kNB) - 1) & 1)) { *failed = 1; break; }
       const uint8_t* wt = sW + size_t(s) * kWBytes;
       uint8_t* bt = sB + size_t(bb) * kBBytes;
@@ -309,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(rowp + ((cc ^ r) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ r) * 16)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
+      mbar_arrive(&wempty[s]);  // this thread's reads of the W stage are done (values in registers)
       fence_async_smem();
       mbar_arrive(&b_full[bb]);
     }
