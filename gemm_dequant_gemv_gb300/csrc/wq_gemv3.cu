@@ -114,6 +114,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       bsum[m] = xsum[m] = 0.f;
       acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
     }
+    // this lane's 4 columns' scale and stored zero: weight-side data, read before the dependency wait
+    const __half* SC = static_cast<const __half*>(a.scales);
+    const __half* ZR = static_cast<const __half*>(a.zeros);
+    float sc[4], zr[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int n = n0 + 4 * lane + c;
+      sc[c] = n < N ? __half2float(SC[n]) : 0.f;
+      zr[c] = n < N ? __half2float(ZR[n]) : 0.f;
+    }
     pdl_wait();
     const uint32_t magic = 0x3F000000u;
 
@@ -185,15 +195,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
     // this warp's share of y: s (sum x' m - B_w) - zero X_w over the k it handled
     // (B_w, X_w: butterfly sums over the lanes, the same value in every lane)
-    const __half* SC = static_cast<const __half*>(a.scales);
-    const __half* ZR = static_cast<const __half*>(a.zeros);
-    float sc[4], zr[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int n = n0 + 4 * lane + c;
-      sc[c] = n < N ? __half2float(SC[n]) : 0.f;
-      zr[c] = n < N ? __half2float(ZR[n]) : 0.f;
-    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       const float b = warp_sum(bsum[m]), x = warp_sum(xsum[m]);
