@@ -253,6 +253,29 @@ def test_wq4_sorted_matches_actorder_oracle(G, M, K, N, g):
     _tol(G.to_f64(y), y_ref, a, "f16")
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_wq4_sorted_bf16(G, M):
+    """The sorted act-order path with bf16 activations and scales (CUDA-core
+    kernel at M = 1, tensor-core kernel at M = 4) against the act-order oracle."""
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    K, N, g = 1024, 392, 128
+    d = syn.make_wq4_actorder(seed=17, M=M, K=K, N=N, group=g)
+    xb = syn.f32_to_bf16_bits(d["x"].astype(np.float32))
+    sb = syn.f32_to_bf16_bits(d["scales"].astype(np.float32))
+    qw, gi = G.dev(d["qweight"]), G.dev(d["g_idx"])
+    qs, perm = torch.empty_like(qw), torch.empty_like(gi)
+    wq.wq4_actorder_prepare(qw, gi, K, N, g, qs, perm)
+    buf, y = G.guarded((M, N), torch.bfloat16)
+    wq.wq4_gemm_sorted(G.dev(xb), qs, G.dev(sb), G.dev(d["qzeros"]), perm, y, M, K, N, g, wq.WQ_BF16)
+    torch.cuda.synchronize()
+    G.check_canary(buf, M * N)
+    import oracle
+    y_ref, a = oracle.wq4_gemm(xb, 1, d["qweight"], sb, d["qzeros"], d["g_idx"], g)
+    _tol(G.to_f64(y), y_ref, a, "bf16")
+
+
 def test_wq4_prepare_rejects_unequal_groups(G):
     import torch
     import gemm_dequant_gemv_gb300 as wq
