@@ -183,6 +183,63 @@ def test_repeat_bit_identical_and_pdl(G):
     assert np.array_equal(G.bits_u16(G.run_wq3(d3)), G.bits_u16(G.run_wq3(d3, flags=wq.WQ_FLAG_PDL)))
 
 
+def test_decode_step_chain_matches_oracle(G):
+    """The benchmark's launch configuration: two layers of [W4 act-order on
+    sorted rows, W8, W3] at full size, chained with programmatic dependent
+    launch in one CUDA graph and replayed twice; every output matches the oracle."""
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    import oracle
+    import synthetic as syn
+    layers = []
+    for l in range(2):
+        d8 = syn.make_wq8(seed=1000 * l + 1)
+        d3 = syn.make_wq3(seed=1000 * l + 2)
+        d4 = syn.make_wq4_actorder(seed=1000 * l + 3)
+        t8 = {k: G.dev(d8[k]) for k in ("x", "w", "scales")}
+        t3 = {k: G.dev(d3[k]) for k in ("x", "mat", "scales", "zeros")}
+        t4 = {k: G.dev(d4[k]) for k in ("x", "qweight", "scales", "qzeros", "g_idx")}
+        qs, perm = torch.empty_like(t4["qweight"]), torch.empty_like(t4["g_idx"])
+        wq.wq4_actorder_prepare(t4["qweight"], t4["g_idx"], 4096, 11008, 128, qs, perm)
+        y8 = torch.empty((1, 4096), dtype=torch.float32, device=G.DEV)
+        y3 = torch.empty((1, 4096), dtype=torch.float16, device=G.DEV)
+        y4 = torch.empty((1, 11008), dtype=torch.float16, device=G.DEV)
+        layers.append((d8, d3, d4, t8, t3, t4, qs, perm, y8, y3, y4))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    P = wq.WQ_FLAG_PDL
+
+    def step():
+        for d8, d3, d4, t8, t3, t4, qs, perm, y8, y3, y4 in layers:
+            wq.wq4_gemm_sorted(t4["x"], qs, t4["scales"], t4["qzeros"], perm, y4, 1, 4096, 11008, 128, wq.WQ_F16,
+                               flags=P, stream=stream)
+            wq.wq8_gemv(t8["x"], t8["w"], t8["scales"], y8, 1, 4096, 4096, 128, flags=P, stream=stream)
+            wq.wq3_gemv(t3["x"], t3["mat"], t3["scales"], t3["zeros"], y3, 1, 4096, 4096, flags=P, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        step()
+    for _ in range(2):
+        for L in layers:  # poison the outputs: the replay must rewrite every element
+            for y in L[8:]:
+                y.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        for d8, d3, d4, t8, t3, t4, qs, perm, y8, y3, y4 in layers:
+            r8, a8 = oracle.wq8_gemv(d8["x"], d8["w"], d8["scales"], 128)
+            _tol(G.to_f64(y8), r8, a8, "f32")
+            r3, a3 = oracle.wq3_gemv(d3["x"].view(np.uint16), d3["mat"], d3["scales"].view(np.uint16),
+                                     d3["zeros"].view(np.uint16))
+            _tol(G.to_f64(y3), r3, a3, "f16")
+            r4, a4 = G.oracle_wq4(d4)
+            _tol(G.to_f64(y4), r4, a4, "f16")
+    assert wq.read_timeout_flag(clear=True) == 0
+
+
 def test_no_timeouts(G):
     import gemm_dequant_gemv_gb300 as wq
     assert wq.read_timeout_flag(clear=True) == 0
