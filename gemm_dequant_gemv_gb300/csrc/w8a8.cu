@@ -18,15 +18,16 @@
 //
 // Kernels: (1) w8a8_quant_kernel, one CTA per row: Sx, the int8 codes (if
 // requested) and fp16 copies of the codes in the workspace; (2)
-// w8a8_mma_kernel, one 128 x 128 output tile per CTA:
-//   warp 8 : TMA of the fp16 code tile of X (128-byte swizzle) and the int8
-//            tile of W [64 k x 128 n] per 64-value k-stage;
-//   warps 0-3 : convert the int8 W tile to fp16 (exact) in the MN-major
-//            128-byte-swizzled layout of the B operand;
-//   warp 9 : four MMAs (M = N = 128, K = 16) per stage into one of two
-//            tensor-memory accumulators (one per 256-value chunk);
-//   warps 4-7 : drain each chunk into int32 and, at the end, write
-//            Y = bf16(Sx * acc * Sw) through shared memory with coalesced stores.
+// w8a8_mma_kernel, one 128 x 128 output tile per CTA, 128-value k stages:
+//   warp 16 : TMA of the int8 W tile (lane 0, before the dependency wait) and
+//             of the fp16 X code tile (lane 1), both 128-byte swizzled;
+//   warps 0-7 : convert the int8 W tile to fp16 (exact) and store it
+//             transposed into tensor memory, where it is the A operand;
+//   warp 17 : eight MMAs (M = N = 128, K = 16) per stage, A from tensor
+//             memory, B = X from shared memory, into one of two tensor-memory
+//             accumulators (one per 256-value chunk of k);
+//   warps 8-15 : drain each chunk into int32 and, at the end, write
+//             Y = bf16(Sx * acc * Sw) through shared memory with coalesced stores.
 #include <algorithm>
 
 #include "../../include/wq.h"
@@ -80,11 +81,12 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
       if (sx != 0.f) c = min(127, max(-127, __float2int_rn(__fdiv_rn(x, sx))));
       q[i] = c;
     }
+    // fp16 copies in the GEMM's operand order: k0 + {0,2}, {4,6}, {1,3}, {5,7}
     uint4 h;
-    h.x = uint32_t(__half_as_ushort(__int2half_rn(q[0]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[1]))) << 16);
-    h.y = uint32_t(__half_as_ushort(__int2half_rn(q[2]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[3]))) << 16);
-    h.z = uint32_t(__half_as_ushort(__int2half_rn(q[4]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[5]))) << 16);
-    h.w = uint32_t(__half_as_ushort(__int2half_rn(q[6]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[7]))) << 16);
+    h.x = uint32_t(__half_as_ushort(__int2half_rn(q[0]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[2]))) << 16);
+    h.y = uint32_t(__half_as_ushort(__int2half_rn(q[4]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[6]))) << 16);
+    h.z = uint32_t(__half_as_ushort(__int2half_rn(q[1]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[3]))) << 16);
+    h.w = uint32_t(__half_as_ushort(__int2half_rn(q[5]))) | (uint32_t(__half_as_ushort(__int2half_rn(q[7]))) << 16);
     *reinterpret_cast<uint4*>(xq16 + size_t(m) * K + k) = h;
     if (xq_out) {
       uint2 b;
@@ -103,83 +105,87 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
 }
 
 // --------------------------------------------------------------------- GEMM --
+// Roles: the tensor core computes D[n, m] = sum_k W[k, n] X[m, k] for a tile of
+// 128 columns n (MMA M, operand A = W^T in tensor memory) by 128 rows m (MMA N,
+// operand B = the fp16 X codes in shared memory, K-major).  W reaches tensor
+// memory straight from registers, so its fp16 copy never passes through shared
+// memory: shared memory carries only the TMA writes of both tiles, the
+// converters' reads of the int8 W tile and the MMA's reads of X.
 constexpr int kBM = 128, kBN = 128, kBK = 128;
 constexpr int kBoxK = 64;                    // values of k per 128-byte-swizzled X box
 constexpr int kChunkStages = 256 / kBK;      // 256 values of k per exact fp32 chunk
-constexpr int kNS = 3, kNB = 2;
-constexpr int kConvWarps = 8;            // int8 -> fp16 converters of the B tile
+// A stage slot s holds the fp16 X codes (shared memory) and the fp16 W^T
+// (tensor memory) of one stage; both are released by one MMA commit.
+constexpr int kNS = 4;
+constexpr int kNSW = 4;                      // int8 W shared-memory ring
+constexpr int kConvGroups = 2;               // converter groups take alternate stages
+constexpr int kConvWarps = 4 * kConvGroups;  // one warp per tensor-memory lane quarter and group
 constexpr int kEpiWarps = 8;             // two per tensor-memory lane quarter, 64 columns each
 constexpr int kThreads = (kConvWarps + kEpiWarps + 2) * 32;
 constexpr int kWarpTMA = kConvWarps + kEpiWarps, kWarpMMA = kWarpTMA + 1;
+constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue thread
-constexpr int kABoxBytes = kBM * kBoxK * 2;  // 16 KB: one X box (128 rows x 64 k)
-constexpr int kABytes = kBM * kBK * 2;       // 32 KB fp16 codes of X per stage (two boxes)
-constexpr int kWBytes = kBK * kBN;           // 16 KB int8 W
-constexpr int kBBytes = kBN * kBK * 2;       // 32 KB fp16 W in the MN-major layout
-// MN-major 128-byte-swizzle atoms of the B operand: 8 rows of k x 64 values of n.
-constexpr uint32_t kAtomK = 1024;                      // byte stride between k-atoms (adjacent)
-constexpr uint32_t kAtomN = (kBK / 8) * kAtomK;        // byte stride between the two n-atoms
-constexpr int kOutStride = kBN * 2 + 16; // padded bf16 output row in shared memory
+constexpr int kEpiCols = kBM / (kEpiWarps / 4);  // accumulator columns (rows m) per epilogue thread
+constexpr int kXBoxBytes = kBM * kBoxK * 2;  // 16 KB: one X box (128 rows x 64 k)
+constexpr int kXBytes = kBM * kBK * 2;       // 32 KB fp16 codes of X per stage (two boxes)
+constexpr int kWBytes = kBK * kBN;           // 16 KB int8 W per stage (128-byte swizzle)
+constexpr uint32_t kDCols = kBM;             // fp32 accumulator columns per buffer
+constexpr uint32_t kACols = kBK / 2;         // 64 columns of fp16 pairs per W^T stage
+constexpr uint32_t kTmemCols = 2 * kDCols + kNS * kACols;  // 512
+constexpr int kOutStride = kBN * 2 + 16;     // padded bf16 output row in shared memory
+static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+static_assert(kEpiCols == 64, "the epilogue loop reads 16-column groups of a 64-column half");
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
 
 struct SmemW8A8 {
-  size_t a, w, b, sw, sx, bars, misc, total;
+  size_t x, w, sx, bars, misc, total;
   __host__ __device__ SmemW8A8() {
     size_t o = 0;
-    a = o;    o += size_t(kNS) * kABytes;     // also the output staging area at the end
-    b = o;    o += size_t(kNB) * kBBytes;
-    w = o;    o += size_t(kNS) * kWBytes;
-    sw = o;   o = align_up(o + kBN * 4, 16);
+    x = o;    o += size_t(kNS) * kXBytes;     // also the output staging area at the end
+    w = o;    o += size_t(kNSW) * kWBytes;
     sx = o;   o = align_up(o + kBM * 4, 16);
-    bars = o; o = align_up(o + size_t(4 * kNS + 2 * kNB + 4) * 8, 16);
+    bars = o; o = align_up(o + size_t(2 * kNS + 2 * kNSW + 4) * 8, 16);
     misc = o; o = align_up(o + 32, 16);
     total = o + 1024;
   }
 };
-
-// MN-major, 128-byte-swizzle descriptor: leading-dimension offset = stride
-// between the 64-wide n-atoms, stride-dimension offset = stride between the
-// 8-row k-atoms.
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((kAtomN >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((kAtomK >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
-}
+static_assert(kBM * kOutStride <= kNS * kXBytes, "the output tile is staged in the X ring");
+static_assert(kNS % kConvGroups == 0, "a stage slot is always refilled by the same converter group");
 
 struct W8A8Args {
   const float* Sw;
   const float* Sx;       // workspace copy written by the quantization kernel
-  void* Y;               // bf16 [M, N]
-  int32_t* acc_out;      // optional
+  void* Y;
+  int32_t* acc_out;
   int M, K, N;
 };
 
+// 4 x 4 byte transpose across the lanes 4i .. 4i + 3 of a warp: lane 4i + j
+// holds word w_j (4 bytes, one per column) and ends with byte j of w_0 .. w_3.
+// Two exchange rounds (lane ^ 2, then lane ^ 1), one byte permute each.
+__device__ __forceinline__ uint32_t quad_transpose(uint32_t w, uint32_t sel1, uint32_t sel2) {
+  const uint32_t y = prmt(w, __shfl_xor_sync(0xffffffffu, w, 2), sel1);
+  return prmt(y, __shfl_xor_sync(0xffffffffu, y, 1), sel2);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    w8a8_mma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
+    w8a8_mma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                     const W8A8Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemW8A8 L;
-  uint8_t* sA = smem + L.a;
-  uint8_t* sB = smem + L.b;
+  uint8_t* sX = smem + L.x;
   uint8_t* sW = smem + L.w;
-  float* sSw = reinterpret_cast<float*>(smem + L.sw);
   float* sSx = reinterpret_cast<float*>(smem + L.sx);
-  // full / empty: the X-code ring (released when the MMA has read a stage);
-  // wfull / wempty: the int8 W ring (released as soon as the converters have read it)
+  // full / empty: stage slots (X codes landed and W^T stored / both read by the MMAs);
+  // wfull / wempty: the int8 W ring (released as soon as the converters have read it);
+  // t_full / t_empty: the two accumulator buffers (one per 256-value chunk of k)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kNS;
   uint64_t* wfull = empty + kNS;
-  uint64_t* wempty = wfull + kNS;
-  uint64_t* b_full = wempty + kNS;
-  uint64_t* b_empty = b_full + kNB;
-  uint64_t* t_full = b_empty + kNB;
+  uint64_t* wempty = wfull + kNSW;
+  uint64_t* t_full = wempty + kNSW;
   uint64_t* t_empty = t_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.misc + 16);
@@ -189,22 +195,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int M = a.M, K = a.K, N = a.N;
   const int nst = (K + kBK - 1) / kBK;  // the tail of the last stage is zero-filled by TMA
   const int nchunks = (nst + kChunkStages - 1) / kChunkStages;
-  constexpr uint32_t kTmemCols = 2 * kBN;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 4 + 1);  // the four converter warps of a group, and the X producer (with bytes)
       mbar_init(&empty[s], 1);
-      mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], kConvWarps * 32);
     }
-    for (int s = 0; s < kNB; ++s) {
-      mbar_init(&b_full[s], kConvWarps * 32);
-      mbar_init(&b_empty[s], 1);
+    for (int s = 0; s < kNSW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&t_full[s], 1);
-      mbar_init(&t_empty[s], kEpiThreads);
+      mbar_init(&t_empty[s], kEpiWarps);
     }
     *failed = 0;
     fence_mbar_init();
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_a = tmem + 2 * kDCols;  // first column of the W^T stages
   pdl_launch_dependents();
 
   if (warp == kWarpTMA) {
@@ -224,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       for (int i = 0; i < nst && !*failed; ++i) {
-        const int s = i % kNS;
-        if (i >= kNS && !mbar_wait(&wempty[s], ((i / kNS) - 1) & 1)) {
+        const int s = i % kNSW;
+        if (i >= kNSW && !mbar_wait(&wempty[s], ((i / kNSW) - 1) & 1)) {
           *failed = 1;
           break;
         }
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sW + size_t(s) * kWBytes, &wmap, &wfull[s], n0, i * kBK, 0ull);
       }
     } else if (lane == 1) {
-      prefetch_tensormap(&amap);
+      prefetch_tensormap(&xmap);
       pdl_wait();
       for (int i = 0; i < nst && !*failed; ++i) {
         const int s = i % kNS;
@@ -241,10 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *failed = 1;
           break;
         }
-        mbar_expect_tx(&full[s], kABytes);
+        mbar_expect_tx(&full[s], kXBytes);
 #pragma unroll
         for (int h = 0; h < kBK / kBoxK; ++h)
-          tma_load_2d(sA + size_t(s) * kABytes + h * kABoxBytes, &amap, &full[s], i * kBK + h * kBoxK, m0, 0ull);
+          tma_load_2d(sX + size_t(s) * kXBytes + h * kXBoxBytes, &xmap, &full[s], i * kBK + h * kBoxK, m0, 0ull);
       }
     } else {
       pdl_wait();
@@ -253,28 +257,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA --
     pdl_wait();
     if (lane == 0) {
-      // fp32 accumulator, fp16 A (K-major) and B (MN-major), M = N = 128
-      const uint32_t idesc = (1u << 4) | (1u << 16) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+      constexpr uint32_t idesc = f16_idesc(kBN, kBM, 0);  // M = 128 columns n, N = 128 rows m, fp16, fp32 acc
       int last = -1;
       for (int i = 0; i < nst; ++i) {
-        const int s = i % kNS, bb = i % kNB, ch = i / kChunkStages, tb = ch & 1;
+        const int s = i % kNS, ch = i / kChunkStages, tb = ch & 1;
         if (i % kChunkStages == 0 && ch >= 2) {
           if (!mbar_wait(&t_empty[tb], ((ch / 2) - 1) & 1)) { *failed = 1; break; }
         }
-        if (!mbar_wait(&b_full[bb], (i / kNB) & 1) || !mbar_wait(&full[s], (i / kNS) & 1)) {
+        if (!mbar_wait(&full[s], (i / kNS) & 1)) {
           *failed = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + size_t(s) * kABytes);
-        const uint32_t b_base = smem_u32(sB + size_t(bb) * kBBytes);
+        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + size_t(s) * kXBytes));
+        const uint32_t acol = tmem_a + s * kACols;
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          mma_f16(tmem + tb * kBN, sw128_kmajor_desc(a_base + (k / (kBoxK / 16)) * kABoxBytes + 32 * (k % (kBoxK / 16))),
-                  sw128_mnmajor_desc(b_base + 2 * kAtomK * k),
-                  idesc, (i % kChunkStages != 0 || k > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + tb * kDCols, acol + 8 * k,
+                     bdesc + uint64_t(((k / (kBoxK / 16)) * kXBoxBytes + 32 * (k % (kBoxK / 16))) >> 4), idesc,
+                     (i % kChunkStages != 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
-        mma_commit(&b_empty[bb]);
         if (i % kChunkStages == kChunkStages - 1 || i == nst - 1) mma_commit(&t_full[tb]);
         last = i;
       }
@@ -282,58 +284,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kConvWarps) {
     // ---------------------------------------------------------- converters --
-    const int t = threadIdx.x;  // 0 .. kConvWarps * 32 - 1
-    for (int i = 0; i < nst; ++i) {
-      const int s = i % kNS, bb = i % kNB;
-      if (!mbar_wait(&wfull[s], (i / kNS) & 1)) { *failed = 1; break; }
-      if (i >= kNB && !mbar_wait(&b_empty[bb], ((i / kNB) - 1) & 1)) { *failed = 1; break; }
-      const uint8_t* wt = sW + size_t(s) * kWBytes;
-      uint8_t* bt = sB + size_t(bb) * kBBytes;
+    // Warp c writes tensor-memory lanes 32 (c % 4) .. (columns n of the tile)
+    // of the stages i with i % kConvGroups == c / 4.  Per block of 8 values of
+    // k, lane 4i + j reads 4 bytes (columns 32 (c % 4) + 4i ..) of rows k0 + 2j
+    // (word A) and k0 + 2j + 1 (word B) of the swizzled int8 tile; a 4 x 4
+    // transpose across the lane quad leaves lane l with column 32 (c % 4) + l of
+    // rows k0, k0+2, k0+4, k0+6 (A) and k0+1, k0+3, k0+5, k0+7 (B).  Each byte
+    // b = q + 128 becomes the fp16 1024 + b and then q exactly.  The columns of
+    // fp16 pairs hold k0 + {0,2}, {4,6}, {1,3}, {5,7}: the quantization kernel
+    // stores the X codes of every 8-value block in that order.
+    const int quarter = warp & 3, group = warp >> 2;
+    const int qi = lane >> 2, qj = lane & 3;
+    const uint32_t sel1 = (qj & 2) ? 0x3276u : 0x5410u;
+    const uint32_t sel2 = (qj & 1) ? 0x3715u : 0x6240u;
+    const int chunk = 2 * quarter + (qi >> 2), cbyte = 4 * (qi & 3);
+    const int offa = ((chunk ^ (2 * qj)) << 4) + cbyte, offb = ((chunk ^ (2 * qj + 1)) << 4) + cbyte;
+    const uint32_t taddr = tmem_a + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int i = group; i < nst; i += kConvGroups) {
+      const int s = i % kNS, ws = i % kNSW;
+      // warp-uniform decisions: the shuffles and tensor-memory stores below need the whole warp
+      if (!__all_sync(0xffffffffu, mbar_wait(&wfull[ws], (i / kNSW) & 1))) { *failed = 1; break; }
+      if (i >= kNS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((i / kNS) - 1) & 1))) { *failed = 1; break; }
+      tc_fence_after();
+      const uint8_t* wt = sW + size_t(ws) * kWBytes + 2 * qj * kBN;
+      uint32_t h[kACols];
 #pragma unroll
-      for (int p = 0; p < (kWBytes / 16) / (kConvWarps * 32); ++p) {
-        // 16-byte chunk (row k, columns 16c..16c+15) of the int8 tile.  Within each
-        // 8-lane phase k % 8 = i runs over 0..7 and c = (i + d) % 8, so that the
-        // loads (chunk c of a 128-byte row) and both swizzled stores (chunk
-        // (2 (c % 4) [+1]) ^ (k % 8)) hit 8 different bank groups.
-        const int q = t + kConvWarps * 32 * p;
-        const int i = q & 7, rest = q >> 3;
-        const int k = 8 * (rest % (kBK / 8)) + i, c = (i + rest / (kBK / 8)) & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(wt + k * kBN + c * 16);
-        const uint32_t w4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-        uint32_t h[8];
+      for (int b = 0; b < kBK / 8; ++b) {
+        uint32_t wa = *reinterpret_cast<const uint32_t*>(wt + 8 * b * kBN + offa);       // row 8b + 2 qj
+        uint32_t wb = *reinterpret_cast<const uint32_t*>(wt + (8 * b + 1) * kBN + offb); // row 8b + 2 qj + 1
+        wa = quad_transpose(wa, sel1, sel2) ^ 0x80808080u;
+        wb = quad_transpose(wb, sel1, sel2) ^ 0x80808080u;
+        const uint32_t p[4] = {prmt(wa, 0x64646464u, 0x4140u), prmt(wa, 0x64646464u, 0x4342u),
+                               prmt(wb, 0x64646464u, 0x4140u), prmt(wb, 0x64646464u, 0x4342u)};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // bytes b = q + 128 -> fp16 1024 + b, minus 1152 -> q exactly
-          h[2 * j] = prmt(w4[j], 0x64646464u, 0x4140u);
-          h[2 * j + 1] = prmt(w4[j], 0x64646464u, 0x4342u);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t d;
-          asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h[j]), "r"(0x64806480u));
-          h[j] = d;
-        }
-        const int ka = k >> 3, r = k & 7, na = c >> 2, cc = 2 * (c & 3);
-        uint8_t* rowp = bt + ka * kAtomK + na * kAtomN + r * 128;
-        *reinterpret_cast<uint4*>(rowp + ((cc ^ r) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ r) * 16)) = make_uint4(h[4], h[5], h[6], h[7]);
+        for (int j = 0; j < 4; ++j)
+          asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h[4 * b + j]) : "r"(p[j]), "r"(0x64806480u));
       }
-      mbar_arrive(&wempty[s]);  // this thread's reads of the W stage are done (values in registers)
-      fence_async_smem();
-      mbar_arrive(&b_full[bb]);
+      // one arrival per warp: many threads arriving on one barrier serialise
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wempty[ws]);  // the warp's reads of the W stage are done (values in registers)
+      tmem_st32(taddr + s * kACols, h);
+      tmem_st32(taddr + s * kACols + 32, h + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
     }
     pdl_wait();
   } else {
     // ------------------------------------------------------------ epilogue --
-    // warp e (0..7): tensor-memory lane quarter e % 4 = tile rows 32 (e % 4) ..,
-    // columns kEpiCols * (e / 4) ..
+    // warp e (0..7): tensor-memory lane quarter e % 4 = tile columns n
+    // 32 (e % 4) .., accumulator columns (tile rows m) kEpiCols * (e / 4) ..
     pdl_wait();
-    const int et = threadIdx.x - kConvWarps * 32;  // 0 .. kEpiThreads - 1
+    const int et = threadIdx.x - kConvThreads;  // 0 .. kEpiThreads - 1
     const int ew = warp - kConvWarps, quarter = ew & 3, half = ew >> 2;
-    const int row = quarter * 32 + lane;            // tensor-memory lane == output row in the tile
+    const int col = quarter * 32 + lane;            // tensor-memory lane == tile column n
     const int cbase = half * kEpiCols;
-    for (int c = et; c < kBN; c += kEpiThreads) sSw[c] = (n0 + c < N) ? a.Sw[n0 + c] : 0.f;
-    if (half == 0) sSx[row] = (m0 + row < M) ? a.Sx[m0 + row] : 0.f;
+    const float sw = (n0 + col < N) ? a.Sw[n0 + col] : 0.f;
+    for (int r = et; r < kBM; r += kEpiThreads) sSx[r] = (m0 + r < M) ? a.Sx[m0 + r] : 0.f;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cbase;
     uint32_t acc[kEpiCols];
 #pragma unroll
@@ -341,43 +349,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     int drained = 0;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int tb = ch & 1;
-      if (!mbar_wait(&t_full[tb], (ch / 2) & 1)) { *failed = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], (ch / 2) & 1))) { *failed = 1; break; }
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < kEpiCols; c0 += 16) {
         float v[16];
-        tmem_ld16(lane_addr + tb * kBN + c0, v);
+        tmem_ld16(lane_addr + tb * kDCols + c0, v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[c0 + j] += __float_as_uint(v[j] + 12582912.0f);
       }
       tc_fence_before();
-      mbar_arrive(&t_empty[tb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&t_empty[tb]);
       ++drained;
     }
     const uint32_t bias = uint32_t(drained) * 0x4B400000u;
-    // Y = bf16(Sx * acc * Sw) staged in shared memory (the X stages are free now)
-    asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // epilogue warps: sSw / sSx complete
-    const float sx = sSx[row];
-    uint8_t* orow = sA + size_t(row) * kOutStride + cbase * 2;
+    // Y = bf16(Sx * acc * Sw) staged in shared memory (the X stages are free now:
+    // the MMA warp saw the last one released before the epilogue's last chunk)
+    asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // epilogue warps: sSx complete
+    uint16_t* ocol = reinterpret_cast<uint16_t*>(sX) + col;
+    const bool col_ok = n0 + col < N;
 #pragma unroll
-    for (int c0 = 0; c0 < kEpiCols; c0 += 8) {
-      uint32_t pk[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int32_t i0 = static_cast<int32_t>(acc[c0 + 2 * j] - bias);
-        const int32_t i1 = static_cast<int32_t>(acc[c0 + 2 * j + 1] - bias);
-        const float f0 = (sx * static_cast<float>(i0)) * sSw[cbase + c0 + 2 * j];
-        const float f1 = (sx * static_cast<float>(i1)) * sSw[cbase + c0 + 2 * j + 1];
-        pk[j] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f0))) |
-                (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f1))) << 16);
-      }
-      *reinterpret_cast<uint4*>(orow + c0 * 2) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      if (a.acc_out && m0 + row < M) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (n0 + cbase + c0 + j < N)
-            a.acc_out[size_t(m0 + row) * N + n0 + cbase + c0 + j] = static_cast<int32_t>(acc[c0 + j] - bias);
-      }
+    for (int c = 0; c < kEpiCols; ++c) {
+      const int r = cbase + c;
+      const int32_t iv = static_cast<int32_t>(acc[c] - bias);
+      const float f = (sSx[r] * static_cast<float>(iv)) * sw;
+      ocol[size_t(r) * (kOutStride / 2)] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+      if (a.acc_out && col_ok && m0 + r < M) a.acc_out[size_t(m0 + r) * N + n0 + col] = iv;
     }
     asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
     // coalesced stores: 16 chunks of 16 bytes per tile row
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = et; q < kBM * (kBN / 8); q += kEpiThreads) {
       const int r = q / (kBN / 8), c = (q % (kBN / 8)) * 8;
       if (m0 + r < M && n0 + c < N)
-        *reinterpret_cast<uint4*>(Y + size_t(m0 + r) * N + n0 + c) = *reinterpret_cast<const uint4*>(sA + size_t(r) * kOutStride + c * 2);
+        *reinterpret_cast<uint4*>(Y + size_t(m0 + r) * N + n0 + c) = *reinterpret_cast<const uint4*>(sX + size_t(r) * kOutStride + c * 2);
     }
   }
 
@@ -439,16 +437,16 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
     if (e != cudaSuccess) return e;
   }
   // 2) GEMM with the fused rescale epilogue (always chained to the quantization kernel)
-  CUtensorMap amap, wmap;
-  if (!encode_tensor_map_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xq16, K, M, size_t(K) * 2, kBoxK, kBM,
+  CUtensorMap xmap, wmap;
+  if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xq16, K, M, size_t(K) * 2, kBoxK, kBM,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, N, K, N, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, N, K, N, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   W8A8Args args{Sw, sx, Y, acc_out, M, K, N};
   const void* kern = reinterpret_cast<const void*>(w8a8_mma_kernel);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
-  void* kargs[] = {&amap, &wmap, &args};
+  void* kargs[] = {&xmap, &wmap, &args};
   return launch_ex(kern, dim3((N + kBN - 1) / kBN, (M + kBM - 1) / kBM), dim3(kThreads), L.total,
                    flags | WQ_FLAG_PDL, stream, kargs);
 }

@@ -114,12 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < kNA; ++s) {
-      mbar_init(&a_full[s], 4 * 32);
+      mbar_init(&a_full[s], 4);  // one arrival per converter warp
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&t_full[s], 1);
-      mbar_init(&t_empty[s], 4 * 32);
+      mbar_init(&t_empty[s], 4);  // one arrival per epilogue warp
     }
     *failed = 0;
     fence_mbar_init();
@@ -209,8 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t h = ACT_BF16 ? (0x4300u | uint32_t(z)) : (0x6400u | uint32_t(z));
         zbias = h | (h << 16);
       }
-      if (!mbar_wait(&full[s], (i / kNS) & 1)) { *failed = 1; break; }
-      if (i >= kNA && !mbar_wait(&a_empty[ab], ((i / kNA) - 1) & 1)) { *failed = 1; break; }
+      // warp-uniform decisions: the warp synchronises before its arrival below
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kNS) & 1))) { *failed = 1; break; }
+      if (i >= kNA && !__all_sync(0xffffffffu, mbar_wait(&a_empty[ab], ((i / kNA) - 1) & 1))) { *failed = 1; break; }
       const uint32_t* wrow = reinterpret_cast<const uint32_t*>(sW + size_t(s) * kPackedStageBytes) + col;
       uint8_t* arow = sA + size_t(ab) * kABytes + size_t(col) * 128;
 #pragma unroll
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(arow + ((r ^ (col & 7)) * 16)) = v;
       }
       fence_async_smem();
-      mbar_arrive(&a_full[ab]);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&a_full[ab]);
     }
     pdl_wait();
   } else {
@@ -241,13 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc = (n < N) ? (ACT_BF16 ? bf16_bits_to_f32(SC[size_t(g0 + gi) * N + n])
                                            : f16_bits_to_f32(SC[size_t(g0 + gi) * N + n]))
                                : 0.f;
-      if (!mbar_wait(&t_full[tb], (gi / 2) & 1)) { *failed = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], (gi / 2) & 1))) { *failed = 1; break; }
       tc_fence_after();
       float d[MP];
 #pragma unroll
       for (int c = 0; c < MP; c += 16) tmem_ld16(lane_addr + tb * MP + c, d + c);
       tc_fence_before();
-      mbar_arrive(&t_empty[tb]);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&t_empty[tb]);
 #pragma unroll
       for (int m = 0; m < MP; ++m) acc[m] = fmaf(sc, d[m], acc[m]);
     }
