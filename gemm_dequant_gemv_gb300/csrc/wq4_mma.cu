@@ -6,15 +6,19 @@
 // The weight side is the MMA's M dimension (swap-AB): one CTA owns 128 output
 // columns, D[n, m] lives in tensor memory (128 lanes x Mp fp32 columns).
 //
-// Per 64-value k-stage:
-//   * warp 8 (TMA) loads the packed int32 words [8 rows x 128 columns] and the
-//     x tile [Mp rows x 64] (128-byte swizzle) into a ring of stages;
-//   * warps 0-3 (converters, one output column per thread) unpack the nibbles
-//     to the exact 16-bit integers q - z (PRMT into 128 + q / 1024 + q, then one
-//     packed subtraction) and write them as the K-major, 128-byte-swizzled A
-//     operand;
-//   * warp 9 issues four kind::f16 MMAs (K = 16 each) per stage into one of
-//     two tensor-memory accumulators, one accumulator per scale group;
+// Per k-stage of KS = 128 values (64 when the group size is not a multiple of
+// 128):
+//   * warp 8 (TMA) loads the packed int32 words [KS/8 rows x 128 columns] and
+//     the x tile [Mp rows x KS] (128-byte-swizzled boxes of 64 values) into a
+//     ring of stages;
+//   * warps 0-3 (converters, one output column per thread = one tensor-memory
+//     lane) unpack the nibbles to the exact 16-bit integers q - z (PRMT into
+//     128 + q / 1024 + q, then one packed subtraction) and store them with
+//     tcgen05.st as the A operand in tensor memory (fp16 pairs of consecutive k
+//     per 32-bit column), so the dequantized weights never touch shared memory;
+//   * warp 9 issues KS/16 kind::f16 MMAs (K = 16 each, A from tensor memory,
+//     B = x from shared memory) per stage into one of two tensor-memory
+//     accumulators, one accumulator per scale group;
 //   * warps 4-7 (epilogue) drain each finished group accumulator and apply the
 //     group's scale in fp32: y += s[g,n] * D_g[n,:].
 // Products (q - z) * x are exact; the only roundings are the fp32 sums.  The K
@@ -38,13 +42,24 @@ int device_max_smem();
 namespace {
 
 constexpr int kBN = 128;            // output columns per tile (MMA M)
-constexpr int kKS = 64;             // values of k per stage
-constexpr int kNS = 6;              // stages in the TMA ring
-constexpr int kNA = 2;              // dequantized A buffers
+constexpr int kBoxK = 64;           // values of k per 128-byte-swizzled x box
+constexpr int kNA = 2;              // dequantized A stages in tensor memory
 constexpr int kWarpTMA = 8, kWarpMMA = 9;
 constexpr int kThreads = 10 * 32;
-constexpr int kPackedStageBytes = (kKS / 8) * kBN * 4;   // 4 KB
-constexpr int kABytes = kBN * kKS * 2;                    // 16 KB
+
+// Per-KS constants: stages in the TMA ring, bytes of packed weights per stage,
+// and the tensor-memory columns (two group accumulators, then the A stages).
+template <int KS> struct Stage {
+  static constexpr int NS = KS == 64 ? 6 : 4;
+  static constexpr int kPacked = (KS / 8) * kBN * 4;  // 4 or 8 KB
+  static constexpr uint32_t kACols = KS / 2;           // fp16 pairs per A stage
+};
+template <int MP, int KS> struct Tmem {
+  static constexpr uint32_t kA = 2 * MP;               // first A column
+  static constexpr uint32_t kUsed = 2 * MP + kNA * Stage<KS>::kACols;
+  static constexpr uint32_t kCols = kUsed <= 32 ? 32 : kUsed <= 64 ? 64 : kUsed <= 128 ? 128 : kUsed <= 256 ? 256 : 512;
+  static_assert(kUsed <= 256, "two CTAs per SM share the 512 tensor-memory columns");
+};
 
 struct MmaArgs {
   void* y;
@@ -56,14 +71,14 @@ struct MmaArgs {
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
 
 struct SmemMma {
-  size_t a, xs, pw, part, bars, misc, total;
-  __host__ __device__ explicit SmemMma(int MP) {
+  size_t xs, pw, part, bars, misc, total;
+  __host__ __device__ SmemMma(int MP, int KS) {
+    const int NS = KS == 64 ? Stage<64>::NS : Stage<128>::NS;
     size_t o = 0;
-    a = o;    o += size_t(kNA) * kABytes;
-    xs = o;   o += size_t(kNS) * MP * 128;
-    pw = o;   o += size_t(kNS) * kPackedStageBytes;
+    xs = o;   o += size_t(NS) * MP * KS * 2;            // x stages (boxes of Mp x 64, 1024-byte multiples)
+    pw = o;   o += size_t(NS) * (KS / 8) * kBN * 4;
     part = o; o = align_up(o + size_t(MP) * kBN * 4, 16);
-    bars = o; o = align_up(o + size_t(2 * kNS + 2 * kNA + 4) * 8, 16);
+    bars = o; o = align_up(o + size_t(2 * NS + 2 * kNA + 4) * 8, 16);
     misc = o; o = align_up(o + 32, 16);
     total = o + 1024;  // slack to align the base to 1024 bytes
   }
@@ -79,14 +94,18 @@ __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
   return d;
 }
 
-template <int MP, int ACT_BF16, bool HAS_Z>
+template <int MP, int ACT_BF16, bool HAS_Z, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     wq4_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const MmaArgs a) {
+  constexpr int kNS = Stage<KS>::NS;
+  constexpr int kPackedStageBytes = Stage<KS>::kPacked;
+  constexpr uint32_t kACols = Stage<KS>::kACols;
+  constexpr int kXStageBytes = MP * KS * 2;
+  constexpr int kXBoxBytes = MP * kBoxK * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemMma L(MP);
-  uint8_t* sA = smem + L.a;
+  const SmemMma L(MP, KS);
   uint8_t* sX = smem + L.xs;
   uint8_t* sW = smem + L.pw;
   float* part = reinterpret_cast<float*>(smem + L.part);
@@ -102,11 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = gridDim.x, n0 = blockIdx.y * kBN;
   const int M = a.M, K = a.K, N = a.N, gsz = a.group;
-  const int spg = gsz / kKS;  // stages per group
+  const int spg = gsz / KS;  // stages per group
   int g0, g1;
   split_range(K / gsz, S, blockIdx.x, g0, g1);
   const int ng = g1 - g0, nst = ng * spg, ks0 = g0 * spg;
-  constexpr uint32_t kTmemCols = (2 * MP < 32) ? 32 : 2 * MP;
+  constexpr uint32_t kTmemCols = Tmem<MP, KS>::kCols;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
@@ -141,16 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
       const uint64_t pol = l2_evict_first_policy();
-      const uint32_t stage_bytes = kPackedStageBytes + MP * 128;
+      const uint32_t stage_bytes = kPackedStageBytes + kXStageBytes;
       const int pre = nst < kNS ? nst : kNS;
       // weights of the first stages before the dependency wait, x after it
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(&full[i], stage_bytes);
-        tma_load_2d(sW + size_t(i) * kPackedStageBytes, &wmap, &full[i], n0, (ks0 + i) * (kKS / 8), pol);
+        tma_load_2d(sW + size_t(i) * kPackedStageBytes, &wmap, &full[i], n0, (ks0 + i) * (KS / 8), pol);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(sX + size_t(i) * MP * 128, &xmap, &full[i], (ks0 + i) * kKS, 0, 0ull);
+#pragma unroll
+        for (int h = 0; h < KS / kBoxK; ++h)
+          tma_load_2d(sX + size_t(i) * kXStageBytes + h * kXBoxBytes, &xmap, &full[i], (ks0 + i) * KS + h * kBoxK, 0, 0ull);
       for (int i = kNS; i < nst && !*failed; ++i) {
         const int s = i % kNS;
         if (!mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
@@ -158,8 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(sW + size_t(s) * kPackedStageBytes, &wmap, &full[s], n0, (ks0 + i) * (kKS / 8), pol);
-        tma_load_2d(sX + size_t(s) * MP * 128, &xmap, &full[s], (ks0 + i) * kKS, 0, 0ull);
+        tma_load_2d(sW + size_t(s) * kPackedStageBytes, &wmap, &full[s], n0, (ks0 + i) * (KS / 8), pol);
+#pragma unroll
+        for (int h = 0; h < KS / kBoxK; ++h)
+          tma_load_2d(sX + size_t(s) * kXStageBytes + h * kXBoxBytes, &xmap, &full[s], (ks0 + i) * KS + h * kBoxK, 0, 0ull);
       }
     } else {
       pdl_wait();
@@ -180,12 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + size_t(ab) * kABytes);
-        const uint32_t b_base = smem_u32(sX + size_t(s) * MP * 128);
+        const uint32_t acol = tmem + Tmem<MP, KS>::kA + ab * kACols;
+        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + size_t(s) * kXStageBytes));
 #pragma unroll
-        for (int k = 0; k < kKS / 16; ++k)
-          mma_f16(tmem + tb * MP, sw128_kmajor_desc(a_base + 32 * k), sw128_kmajor_desc(b_base + 32 * k), idesc,
-                  (i % spg != 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < KS / 16; ++k)
+          mma_f16_ts(tmem + tb * MP, acol + 8 * k,
+                     bdesc + uint64_t(((k / (kBoxK / 16)) * kXBoxBytes + 32 * (k % (kBoxK / 16))) >> 4), idesc,
+                     (i % spg != 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
         mma_commit(&a_empty[ab]);
         if (i % spg == spg - 1) mma_commit(&t_full[tb]);
@@ -213,20 +237,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kNS) & 1))) { *failed = 1; break; }
       if (i >= kNA && !__all_sync(0xffffffffu, mbar_wait(&a_empty[ab], ((i / kNA) - 1) & 1))) { *failed = 1; break; }
       const uint32_t* wrow = reinterpret_cast<const uint32_t*>(sW + size_t(s) * kPackedStageBytes) + col;
-      uint8_t* arow = sA + size_t(ab) * kABytes + size_t(col) * 128;
+      tc_fence_after();
+      uint32_t h[kACols];
 #pragma unroll
-      for (int r = 0; r < kKS / 8; ++r) {
+      for (int r = 0; r < KS / 8; ++r) {
         const uint32_t w = wrow[r * kBN];
         const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
         const uint32_t c0123 = prmt(lo, hi, 0x5140u), c4567 = prmt(lo, hi, 0x7362u);
-        uint4 v;
-        v.x = sub2<ACT_BF16>(prmt(c0123, magic, 0x4140u), zbias);
-        v.y = sub2<ACT_BF16>(prmt(c0123, magic, 0x4342u), zbias);
-        v.z = sub2<ACT_BF16>(prmt(c4567, magic, 0x4140u), zbias);
-        v.w = sub2<ACT_BF16>(prmt(c4567, magic, 0x4342u), zbias);
-        *reinterpret_cast<uint4*>(arow + ((r ^ (col & 7)) * 16)) = v;
+        h[4 * r + 0] = sub2<ACT_BF16>(prmt(c0123, magic, 0x4140u), zbias);
+        h[4 * r + 1] = sub2<ACT_BF16>(prmt(c0123, magic, 0x4342u), zbias);
+        h[4 * r + 2] = sub2<ACT_BF16>(prmt(c4567, magic, 0x4140u), zbias);
+        h[4 * r + 3] = sub2<ACT_BF16>(prmt(c4567, magic, 0x4342u), zbias);
       }
-      fence_async_smem();
+      // this warp's lane quarter (columns 32 w ..) of the A stage
+      const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + Tmem<MP, KS>::kA + ab * kACols;
+#pragma unroll
+      for (int c = 0; c < int(kACols); c += 32) tmem_st32(taddr + c, h + c);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(&a_full[ab]);
     }
@@ -270,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   });
 }
 
-template <int MP, int ACT, bool HZ>
+template <int MP, int ACT, bool HZ, int KS>
 cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaArgs& a, int T, int S,
                        unsigned flags, cudaStream_t stream) {
-  const void* kern = reinterpret_cast<const void*>(wq4_mma_kernel<MP, ACT, HZ>);
-  const size_t smem = SmemMma(MP).total;
+  const void* kern = reinterpret_cast<const void*>(wq4_mma_kernel<MP, ACT, HZ, KS>);
+  const size_t smem = SmemMma(MP, KS).total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -302,13 +330,19 @@ cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const M
   return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
-template <int MP>
+template <int MP, int KS>
 cudaError_t dispatch_mp(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaArgs& a, int T, int S,
                         int act_bf16, bool has_z, unsigned flags, cudaStream_t stream) {
-  if (act_bf16) return has_z ? launch_mma<MP, 1, true>(wmap, xmap, a, T, S, flags, stream)
-                             : launch_mma<MP, 1, false>(wmap, xmap, a, T, S, flags, stream);
-  return has_z ? launch_mma<MP, 0, true>(wmap, xmap, a, T, S, flags, stream)
-               : launch_mma<MP, 0, false>(wmap, xmap, a, T, S, flags, stream);
+  if (act_bf16) return has_z ? launch_mma<MP, 1, true, KS>(wmap, xmap, a, T, S, flags, stream)
+                             : launch_mma<MP, 1, false, KS>(wmap, xmap, a, T, S, flags, stream);
+  return has_z ? launch_mma<MP, 0, true, KS>(wmap, xmap, a, T, S, flags, stream)
+               : launch_mma<MP, 0, false, KS>(wmap, xmap, a, T, S, flags, stream);
+}
+template <int MP>
+cudaError_t dispatch_ks(int KS, const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaArgs& a, int T, int S,
+                        int act_bf16, bool has_z, unsigned flags, cudaStream_t stream) {
+  return KS == 128 ? dispatch_mp<MP, 128>(wmap, xmap, a, T, S, act_bf16, has_z, flags, stream)
+                   : dispatch_mp<MP, 64>(wmap, xmap, a, T, S, act_bf16, has_z, flags, stream);
 }
 
 }  // namespace
@@ -316,30 +350,31 @@ cudaError_t dispatch_mp(const CUtensorMap& wmap, const CUtensorMap& xmap, const 
 cudaError_t launch_wq4_mma(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
                            void* y, int M, int K, int N, int group, int act_bf16, unsigned flags,
                            cudaStream_t stream) {
-  if (group % kKS != 0) return cudaErrorNotSupported;
+  if (group % kBoxK != 0) return cudaErrorNotSupported;
+  const int KS = group % 128 == 0 ? 128 : 64;  // one or more whole stages per scale group
   const int T = (N + kBN - 1) / kBN, units = K / group;
   const int sms = std::max(1, device_sm_count());
   int S = std::max(1, std::min(8, (sms + T / 2) / T));
   S = std::min(S, units);
   CUtensorMap wmap;
-  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, kBN, kKS / 8,
+  if (!encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N, K / 8, size_t(N) * 4, kBN, KS / 8,
                             CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   for (int m0 = 0; m0 < M; m0 += 64) {
     const int mc = std::min(64, M - m0);
     const int MP = mc <= 16 ? 16 : (mc <= 32 ? 32 : 64);
-    if (SmemMma(MP).total > static_cast<size_t>(device_max_smem())) return cudaErrorNotSupported;
+    if (SmemMma(MP, KS).total > static_cast<size_t>(device_max_smem())) return cudaErrorNotSupported;
     CUtensorMap xmap;
     const uint16_t* xc = static_cast<const uint16_t*>(x) + size_t(m0) * K;
-    if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, xc, K, mc, size_t(K) * 2, kKS, MP,
+    if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, xc, K, mc, size_t(K) * 2, kBoxK, MP,
                               CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     MmaArgs args{static_cast<uint16_t*>(y) + size_t(m0) * N, scales, qzeros, mc, K, N, group};
     cudaError_t e;
     switch (MP) {
-      case 16: e = dispatch_mp<16>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
-      case 32: e = dispatch_mp<32>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
-      default: e = dispatch_mp<64>(wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+      case 16: e = dispatch_ks<16>(KS, wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+      case 32: e = dispatch_ks<32>(KS, wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
+      default: e = dispatch_ks<64>(KS, wmap, xmap, args, T, S, act_bf16, qzeros != nullptr, flags, stream); break;
     }
     if (e != cudaSuccess) return e;
   }
