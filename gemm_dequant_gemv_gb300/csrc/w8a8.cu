@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&wmap);
       for (int i = 0; i < nst && !*failed; ++i) {
         const int s = i % kNSW;
-        if (i >= kNSW && !mbar_wait(&wempty[s], ((i / kNSW) - 1) & 1)) {
+        if (i >= kNSW && !mbar_wait_sleep(&wempty[s], ((i / kNSW) - 1) & 1)) {
           *failed = 1;
           break;
         }
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait();
       for (int i = 0; i < nst && !*failed; ++i) {
         const int s = i % kNS;
-        if (i >= kNS && !mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
+        if (i >= kNS && !mbar_wait_sleep(&empty[s], ((i / kNS) - 1) & 1)) {
           *failed = 1;
           break;
         }
@@ -262,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nst; ++i) {
         const int s = i % kNS, ch = i / kChunkStages, tb = ch & 1;
         if (i % kChunkStages == 0 && ch >= 2) {
-          if (!mbar_wait(&t_empty[tb], ((ch / 2) - 1) & 1)) { *failed = 1; break; }
+          if (!mbar_wait_sleep(&t_empty[tb], ((ch / 2) - 1) & 1)) { *failed = 1; break; }
         }
-        if (!mbar_wait(&full[s], (i / kNS) & 1)) {
+        if (!mbar_wait_sleep(&full[s], (i / kNS) & 1)) {
           *failed = 1;
           break;
         }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i % kChunkStages == kChunkStages - 1 || i == nst - 1) mma_commit(&t_full[tb]);
         last = i;
       }
-      if (last >= 0) mbar_wait(&empty[last % kNS], (last / kNS) & 1);
+      if (last >= 0) mbar_wait_sleep(&empty[last % kNS], (last / kNS) & 1);
     }
   } else if (warp < kConvWarps) {
     // ---------------------------------------------------------- converters --
@@ -303,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = group; i < nst; i += kConvGroups) {
       const int s = i % kNS, ws = i % kNSW;
       // warp-uniform decisions: the shuffles and tensor-memory stores below need the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait(&wfull[ws], (i / kNSW) & 1))) { *failed = 1; break; }
-      if (i >= kNS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((i / kNS) - 1) & 1))) { *failed = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&wfull[ws], (i / kNSW) & 1))) { *failed = 1; break; }
+      if (i >= kNS && !__all_sync(0xffffffffu, mbar_wait_sleep(&empty[s], ((i / kNS) - 1) & 1))) { *failed = 1; break; }
       tc_fence_after();
       const uint8_t* wt = sW + size_t(ws) * kWBytes + 2 * qj * kBN;
       uint32_t h[kACols];
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int drained = 0;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int tb = ch & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], (ch / 2) & 1))) { *failed = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&t_full[tb], (ch / 2) & 1))) { *failed = 1; break; }
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < kEpiCols; c0 += 16) {

@@ -46,6 +46,7 @@ constexpr int kBoxK = 64;           // values of k per 128-byte-swizzled x box
 constexpr int kNA = 2;              // dequantized A stages in tensor memory
 constexpr int kWarpTMA = 8, kWarpMMA = 9;
 constexpr int kThreads = 10 * 32;
+constexpr int kPf = 8;              // scale groups whose scales / zeros are fetched ahead
 
 // Per-KS constants: stages in the TMA ring, bytes of packed weights per stage,
 // and the tensor-memory columns (two group accumulators, then the A stages).
@@ -95,7 +96,7 @@ __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
 }
 
 template <int MP, int ACT_BF16, bool HAS_Z, int KS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, MP <= 32 ? 2 : 1)  // two CTAs per SM up to Mp = 32
     wq4_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const MmaArgs a) {
   constexpr int kNS = Stage<KS>::NS;
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sX + size_t(i) * kXStageBytes + h * kXBoxBytes, &xmap, &full[i], (ks0 + i) * KS + h * kBoxK, 0, 0ull);
       for (int i = kNS; i < nst && !*failed; ++i) {
         const int s = i % kNS;
-        if (!mbar_wait(&empty[s], ((i / kNS) - 1) & 1)) {
+        if (!mbar_wait_sleep(&empty[s], ((i / kNS) - 1) & 1)) {
           *failed = 1;
           break;
         }
@@ -196,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nst; ++i) {
         const int s = i % kNS, ab = i % kNA, gi = i / spg, tb = gi & 1;
         if (i % spg == 0 && gi >= 2) {
-          if (!mbar_wait(&t_empty[tb], ((gi / 2) - 1) & 1)) { *failed = 1; break; }
+          if (!mbar_wait_sleep(&t_empty[tb], ((gi / 2) - 1) & 1)) { *failed = 1; break; }
         }
-        if (!mbar_wait(&a_full[ab], (i / kNA) & 1) || !mbar_wait(&full[s], (i / kNS) & 1)) {
+        if (!mbar_wait_sleep(&a_full[ab], (i / kNA) & 1) || !mbar_wait_sleep(&full[s], (i / kNS) & 1)) {
           *failed = 1;
           break;
         }
@@ -216,26 +217,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         last = i;
       }
       // the tensor memory is released only after the last MMA has completed
-      if (last >= 0) mbar_wait(&empty[last % kNS], (last / kNS) & 1);
+      if (last >= 0) mbar_wait_sleep(&empty[last % kNS], (last / kNS) & 1);
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------- converters --
     const int col = threadIdx.x;  // 0..127
     const int n = n0 + col;
     const uint32_t magic = ACT_BF16 ? 0x43434343u : 0x64646464u;
+    // packed zeros: weight-side data fetched a chunk of kPf groups ahead, so a
+    // load has kPf groups of time to land before its group starts
+    auto zero_word = [&](int gi) -> uint32_t {
+      return (HAS_Z && n < N && gi < ng) ? static_cast<uint32_t>(a.qzeros[size_t(g0 + gi) * (N / 8) + n / 8]) : 0u;
+    };
+    uint32_t zcur[kPf], znxt[kPf];
+    if (HAS_Z) {
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) {
+        zcur[j] = zero_word(j);
+        znxt[j] = zero_word(kPf + j);
+      }
+    }
     uint32_t zbias = 0;
     for (int i = 0; i < nst; ++i) {
       const int s = i % kNS, ab = i % kNA;
       if (i % spg == 0) {
+        const int gi = i / spg;
         int z = 8;
-        if (HAS_Z && n < N) z = (a.qzeros[size_t(g0 + i / spg) * (N / 8) + n / 8] >> (4 * (n % 8))) & 15;
+        if (HAS_Z) {
+          if (gi % kPf == 0 && gi > 0) {
+#pragma unroll
+            for (int j = 0; j < kPf; ++j) {
+              zcur[j] = znxt[j];
+              znxt[j] = zero_word(gi + kPf + j);
+            }
+          }
+          if (n < N) z = (zcur[gi % kPf] >> (4 * (n % 8))) & 15;
+        }
         // 16-bit pair of (128 + z) in bf16 or (1024 + z) in fp16
         const uint32_t h = ACT_BF16 ? (0x4300u | uint32_t(z)) : (0x6400u | uint32_t(z));
         zbias = h | (h << 16);
       }
       // warp-uniform decisions: the warp synchronises before its arrival below
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kNS) & 1))) { *failed = 1; break; }
-      if (i >= kNA && !__all_sync(0xffffffffu, mbar_wait(&a_empty[ab], ((i / kNA) - 1) & 1))) { *failed = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&full[s], (i / kNS) & 1))) { *failed = 1; break; }
+      if (i >= kNA && !__all_sync(0xffffffffu, mbar_wait_sleep(&a_empty[ab], ((i / kNA) - 1) & 1))) { *failed = 1; break; }
       const uint32_t* wrow = reinterpret_cast<const uint32_t*>(sW + size_t(s) * kPackedStageBytes) + col;
       tc_fence_after();
       uint32_t h[kACols];
@@ -261,26 +285,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
   } else {
     // ------------------------------------------------------------ epilogue --
-    pdl_wait();
     const int col = threadIdx.x - 4 * 32;  // 0..127 == tensor-memory lane
     const int n = n0 + col;
     const uint16_t* SC = static_cast<const uint16_t*>(a.scales);
+    // group scales: weight-side data, read before the dependency wait and then a
+    // chunk of kPf groups ahead of their use (the loads come from HBM)
+    auto scale_bits = [&](int gi) -> uint32_t {
+      return (n < N && gi < ng) ? static_cast<uint32_t>(SC[size_t(g0 + gi) * N + n]) : 0u;
+    };
+    uint32_t cur[kPf], nxt[kPf];
+#pragma unroll
+    for (int j = 0; j < kPf; ++j) cur[j] = scale_bits(j);
+    pdl_wait();
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    for (int gi = 0; gi < ng; ++gi) {
-      const int tb = gi & 1;
-      const float sc = (n < N) ? (ACT_BF16 ? bf16_bits_to_f32(SC[size_t(g0 + gi) * N + n])
-                                           : f16_bits_to_f32(SC[size_t(g0 + gi) * N + n]))
-                               : 0.f;
-      if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], (gi / 2) & 1))) { *failed = 1; break; }
-      tc_fence_after();
-      float d[MP];
+    bool stop = false;
+    for (int gb = 0; gb < ng && !stop; gb += kPf) {
 #pragma unroll
-      for (int c = 0; c < MP; c += 16) tmem_ld16(lane_addr + tb * MP + c, d + c);
-      tc_fence_before();
-      __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&t_empty[tb]);
+      for (int j = 0; j < kPf; ++j) nxt[j] = scale_bits(gb + kPf + j);
 #pragma unroll
-      for (int m = 0; m < MP; ++m) acc[m] = fmaf(sc, d[m], acc[m]);
+      for (int j = 0; j < kPf; ++j) {
+        const int gi = gb + j;
+        if (gi >= ng) break;
+        const int tb = gi & 1;
+        const float sc = ACT_BF16 ? bf16_bits_to_f32(cur[j]) : f16_bits_to_f32(cur[j]);
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&t_full[tb], (gi / 2) & 1))) {
+          *failed = 1;
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        float d[MP];
+#pragma unroll
+        for (int c = 0; c < MP; c += 16) tmem_ld16(lane_addr + tb * MP + c, d + c);
+        tc_fence_before();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&t_empty[tb]);
+#pragma unroll
+        for (int m = 0; m < MP; ++m) acc[m] = fmaf(sc, d[m], acc[m]);
+      }
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) cur[j] = nxt[j];
     }
 #pragma unroll
     for (int m = 0; m < MP; ++m) part[m * kBN + col] = acc[m];

