@@ -7,9 +7,10 @@
 //   Y[m,n]   = bf16(Sx[m] * acc[m,n] * Sw[n])      (rescale fused into the matmul epilogue)
 //
 // sm_103a has no integer tcgen05 MMA, so the product runs as kind::f16 on
-// fp16 operands that hold the integer codes exactly (|q| <= 127).  Every
+// fp16 operands that hold the integer codes exactly (X codes in [-127, 127],
+// weights in [-128, 127]).  Every
 // product is an exact integer and so is every partial sum below 2^24: the
-// tensor core accumulates 256 values of k (|sum| <= 256 * 127^2 < 2^22) into
+// tensor core accumulates 256 values of k (|sum| <= 256 * 127 * 128 < 2^22) into
 // an fp32 tensor-memory accumulator, and the epilogue warps fold each such
 // chunk into an int32 register sum with the magic-number conversion
 // bits(f + 1.5 * 2^23) (exact for |f| < 2^22; the constant is removed once at

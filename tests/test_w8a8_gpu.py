@@ -62,7 +62,9 @@ def test_w8a8_parity_small(G, M, K, N):
 
 
 def test_w8a8_adversarial_full_magnitude(G):
-    """Every code +-127 with aligned signs: |acc| = K * 127^2 (132 M at K = 8192)."""
+    """Every code of X +-127 with aligned signs: |acc| up to K * 127 * 128 (133 M at
+    K = 8192) with W = -128 in some columns, the edge of the exact 256-value chunk
+    (256 * 127 * 128 < 2^22)."""
     import synthetic as syn
     M, K, N = 128, 8192, 256
     Xf = np.full((M, K), 2.0, np.float32)
@@ -70,6 +72,7 @@ def test_w8a8_adversarial_full_magnitude(G):
     Xf[5] = 0.0                          # an all-zero row
     W = np.full((K, N), 127, np.int8)
     W[:, 1::3] = -127
+    W[:, 2::5] = -128
     Sw = np.full((N,), 0.01, np.float32)
     _check(G, syn.f32_to_bf16_bits(Xf), W, Sw)
 
