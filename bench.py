@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the roofline kernel
 # (k4_gemv_kernel, sorted rows, 4096 x 11008, M = 1), from one ncu --set full capture
 # of that kernel under this script's own command; set to None when that kernel changes.
-K4_SORTED_TRAFFIC_BYTES = 23478784
+K4_SORTED_TRAFFIC_BYTES = 23479808
 
 
 def alg_bytes_w8(M=1, K=4096, N=4096, g=128):

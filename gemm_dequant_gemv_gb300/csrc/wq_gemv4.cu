@@ -26,7 +26,7 @@ constexpr int kUnitRows = 4;      // packed rows per consumer unit (32 values of
 constexpr int kStageRows = kConsumerWarps * kUnitRows;
 constexpr int kStageK = kStageRows * 8;            // 256 values of k per stage
 constexpr int kStageBytes = kStageRows * kBN * 4;  // 16 KB
-constexpr int kNS = 4;
+constexpr int kNS = 3;  // two CTAs (bound by registers) leave room on the SM for the next kernel's first CTA
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
