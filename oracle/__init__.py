@@ -86,6 +86,12 @@ def _bind(lib):
     lib.wqo_wq3_gemv.argtypes = [P, P, P, P, I, I, I, P, I, P, P]
     lib.wqo_wq4_gemm.restype = None
     lib.wqo_wq4_gemm.argtypes = [P, I, P, P, P, P, I, I, I, I, P, I, P, P]
+    lib.wqo_wq8_dequant.restype = None
+    lib.wqo_wq8_dequant.argtypes = [P, P, I, I, I, P]
+    lib.wqo_wq3_dequant.restype = None
+    lib.wqo_wq3_dequant.argtypes = [P, P, P, I, I, P]
+    lib.wqo_wq4_dequant.restype = None
+    lib.wqo_wq4_dequant.argtypes = [I, P, P, P, P, I, I, I, P]
     lib.wqo_w8a8_quant_rows.restype = None
     lib.wqo_w8a8_quant_rows.argtypes = [P, I, I, P, P]
     lib.wqo_w8a8_gemm_rows.restype = I
@@ -234,6 +240,44 @@ def wq4_gemm(x_bits, act_bf16, qweight, scales_bits, qzeros, g_idx, group, cols=
     _load().wqo_wq4_gemm(_ptr(x), int(bool(act_bf16)), _ptr(qweight), _ptr(scales), _ptr(qz), _ptr(gi),
                          M, K, N, group, _ptr(c), nc, _ptr(y), _ptr(a))
     return y, a
+
+
+# ---- dequantization (dense weights, the unfused baseline) -------------------
+
+def wq8_dequant(w, scales, group):
+    """Exact w(k,n) = scales[k/group, n] * q[k,n] as float64 [K, N]."""
+    w = _c(w, np.int8); scales = _c(scales, np.float32)
+    K, N = w.shape
+    assert K % group == 0 and scales.shape == (K // group, N)
+    out = np.empty((K, N))
+    _load().wqo_wq8_dequant(_ptr(w), _ptr(scales), K, N, group, _ptr(out))
+    return out
+
+
+def wq3_dequant(mat, scales_bits, zeros_bits, K):
+    """Exact w(k,n) = s[n] * q(k,n) - zero[n] (fp16 scale and stored zero) as float64 [K, N]."""
+    mat = _c(mat, np.int32); scales = _c(scales_bits, np.uint16); zeros = _c(zeros_bits, np.uint16)
+    R, N = mat.shape
+    assert K % 32 == 0 and R == 3 * K // 32 and scales.shape == (N,) and zeros.shape == (N,)
+    out = np.empty((K, N))
+    _load().wqo_wq3_dequant(_ptr(mat), _ptr(scales), _ptr(zeros), K, N, _ptr(out))
+    return out
+
+
+def wq4_dequant(act_bf16, qweight, scales_bits, qzeros, g_idx, group):
+    """Exact w(k,n) = s[g(k), n] * (q(k,n) - z[g(k), n]) as float64 [K, N]."""
+    qweight = _c(qweight, np.int32); scales = _c(scales_bits, np.uint16)
+    R, N = qweight.shape
+    K = 8 * R
+    assert K % group == 0 and scales.shape == (K // group, N)
+    qz = None if qzeros is None else _c(qzeros, np.int32)
+    gi = None if g_idx is None else _c(g_idx, np.int32)
+    if gi is not None:
+        assert gi.shape == (K,) and gi.min() >= 0 and gi.max() < K // group
+    out = np.empty((K, N))
+    _load().wqo_wq4_dequant(int(bool(act_bf16)), _ptr(qweight), _ptr(scales), _ptr(qz), _ptr(gi), K, N, group,
+                            _ptr(out))
+    return out
 
 
 def w8a8_quant_rows(X_bits):

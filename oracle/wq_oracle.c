@@ -233,6 +233,43 @@ void wqo_wq4_gemm(const uint16_t* x, int act_bf16, const int32_t* qweight,
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Dequantization to a dense matrix (the separate-kernel path of            */
+/* "融合反量化与GEMM", 核心优化思路: INT8 weights -> a dense buffer in DRAM ->  */
+/* GEMM).  Each value is w(k,n) of the products above, exactly.             */
+/* ------------------------------------------------------------------------ */
+
+void wqo_wq8_dequant(const int8_t* w, const float* scales, int K, int N, int group, double* out) {
+  for (int k = 0; k < K; ++k) {
+    const float* srow = scales + (size_t)(k / group) * N;
+    const int8_t* qrow = w + (size_t)k * N;
+    for (int n = 0; n < N; ++n) out[(size_t)k * N + n] = (double)srow[n] * (double)qrow[n];
+  }
+}
+
+void wqo_wq3_dequant(const int32_t* mat, const uint16_t* scales, const uint16_t* zeros,
+                     int K, int N, double* out) {
+  for (int k = 0; k < K; ++k)
+    for (int n = 0; n < N; ++n) {
+      double s = wqo_f16_to_double(scales[n]);
+      out[(size_t)k * N + n] = s * (double)wqo_code3(mat, N, k, n) - wqo_f16_to_double(zeros[n]);
+    }
+}
+
+void wqo_wq4_dequant(int act_bf16, const int32_t* qweight, const uint16_t* scales,
+                     const int32_t* qzeros, const int32_t* g_idx, int K, int N, int group,
+                     double* out) {
+  double (*dec)(uint16_t) = act_bf16 ? wqo_bf16_to_double : wqo_f16_to_double;
+  for (int k = 0; k < K; ++k) {
+    int grp = g_idx ? g_idx[k] : k / group;
+    for (int n = 0; n < N; ++n) {
+      int zp = qzeros ? wqo_zero4(qzeros, N, grp, n) : 8;
+      int q = wqo_code4(qweight, N, k, n);
+      out[(size_t)k * N + n] = dec(scales[(size_t)grp * N + n]) * (double)(q - zp);
+    }
+  }
+}
+
 void wqo_w8a8_quant_rows(const uint16_t* X, int M, int K, int8_t* Xq, float* Sx) {
   /* [QC] Dynamic Quantization: activations are quantized at run time;
    * 量化粒度 (per-token): one scale per activation row. */

@@ -69,6 +69,16 @@ void wqo_wq3_gemv(const uint16_t* x, const int32_t* mat, const uint16_t* scales,
                   const uint16_t* zeros, int M, int K, int N,
                   const int32_t* cols, int ncols, double* y, double* abs_sum);
 
+/* ---- dequantization (the unfused baseline: dense weights in memory) -------
+ * The exact value of every weight, w(k,n) by the formulas of the products
+ * below, as a dense row-major [K, N] double matrix. */
+void wqo_wq8_dequant(const int8_t* w, const float* scales, int K, int N, int group, double* out);
+void wqo_wq3_dequant(const int32_t* mat, const uint16_t* scales, const uint16_t* zeros,
+                     int K, int N, double* out);
+void wqo_wq4_dequant(int act_bf16, const int32_t* qweight, const uint16_t* scales,
+                     const int32_t* qzeros, const int32_t* g_idx, int K, int N, int group,
+                     double* out);
+
 /* 4-bit, group-wise scales [K/group, N] in the activation dtype, 4-bit zeros
  * [K/group, N/8] (NULL: every zero is 8), optional act-order g_idx [K]
  * (NULL: group of row k is k/group):

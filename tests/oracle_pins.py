@@ -274,6 +274,62 @@ def pin_wq4_invariants():
     assert np.allclose(yb16, ref, rtol=1e-12, atol=1e-12)
 
 
+# ----------------------------------------------------------- dequantization ----
+
+def pin_dequant_hand():
+    """The hand-worked products, recomputed as x . (dense dequantized W) with numpy."""
+    gm = _golden_map("products_small.txt")
+    q = np.array([[1, -2], [3, 4], [-5, 6], [7, -8]], dtype=np.int8)
+    s = np.array([[0.5, 0.25], [2, 1]], dtype=np.float32)
+    x = np.array([[1, 2, 3, 4]], dtype=np.float64)
+    assert (x @ oracle.wq8_dequant(q, s, 2)).tolist() == [[float(v) for v in gm["wq8"][0].split()]]
+    j = np.arange(32)
+    codes3 = np.stack([j % 8, 7 - (j % 8)], axis=1).astype(np.uint8)
+    w3 = oracle.wq3_dequant(syn.pack3(codes3), _f16_bits([0.5, 0.25]), _f16_bits([0.25, 1.0]), 32)
+    assert w3.sum(axis=0).tolist() == [float(v) for v in gm["wq3_ones"][0].split()]
+    assert w3[10].tolist() == [float(v) for v in gm["wq3_e10"][0].split()]
+    for key, ao in (("wq4_plain", False), ("wq4_actorder", True)):
+        xb, qw, sb, qz, gi, g = _wq4_hand_inputs(ao)
+        w4 = oracle.wq4_dequant(0, qw, sb, qz, gi if ao else None, g)
+        y = np.asarray(xb, np.uint16).view(np.float16).astype(np.float64) @ w4
+        assert [y[0, 0], y[0, 7]] == [float(v) for v in gm[key][0].split()], (key, y)
+
+
+def pin_dequant_closed_forms():
+    """Against the hand-worked packed words and the generator's own codes:
+    w = s * (q - z) (4-bit), s * q - zero (3-bit), s[g_idx[k]] rows (act-order)."""
+    zrow = [r for r in read_golden("pack4_words.txt") if r[0] == "zeros"][0]
+    zeros = np.array([int(v) for v in zrow[1].split()], dtype=np.float64)  # columns 0..7
+    zword = np.array([int(zrow[2], 16)], dtype=np.uint64).astype(np.uint32).view(np.int32).reshape(1, 1)
+    for kind, codes, word in read_golden("pack4_words.txt"):
+        if kind != "weight":
+            continue
+        c = np.array([int(v) for v in codes.split()], dtype=np.float64)
+        wd = np.array([int(word, 16)], dtype=np.uint64).astype(np.uint32).view(np.int32)
+        qw = np.repeat(wd.reshape(1, 1), 8, axis=1)
+        got = oracle.wq4_dequant(0, qw, _f16_bits(np.full((1, 8), 0.5)), zword, None, 8)
+        assert np.array_equal(got, 0.5 * (c[:, None] - zeros[None, :])), (codes, got)
+    for label, codes, words in read_golden("pack3_words.txt"):
+        c = np.array([int(v) for v in codes.split()], dtype=np.float64)
+        wd = np.array([int(w, 16) for w in words.split()], dtype=np.uint64).astype(np.uint32).view(np.int32)
+        got = oracle.wq3_dequant(wd.reshape(3, 1), _f16_bits([0.25]), _f16_bits([0.125]), 32)
+        assert np.array_equal(got[:, 0], 0.25 * c - 0.125), label
+    r = _rng(21)
+    K, N, g = 64, 16, 16
+    G = K // g
+    codes = r.integers(0, 16, (K, N), dtype=np.uint8)
+    z = r.integers(0, 16, (G, N), dtype=np.uint8)
+    s = r.uniform(0.005, 0.05, (G, N)).astype(np.float16)
+    gi = syn.gidx_from_permutation(syn.permutation(5, 1, K), g)
+    got = oracle.wq4_dequant(0, syn.pack4(codes), s.view(np.uint16), syn.pack_zeros4(z), gi, g)
+    want = s.astype(np.float64)[gi] * (codes.astype(np.float64) - z.astype(np.float64)[gi])
+    assert np.array_equal(got, want)
+    q8 = r.integers(-128, 128, (K, N), dtype=np.int8)
+    s8 = r.uniform(0.01, 0.02, (G, N)).astype(np.float32)
+    got8 = oracle.wq8_dequant(q8, s8, g)
+    assert np.array_equal(got8, np.repeat(s8.astype(np.float64), g, axis=0) * q8.astype(np.float64))
+
+
 # ------------------------------------------------------------------ w8a8 ----
 
 def pin_w8a8_hand():

@@ -33,6 +33,12 @@ MUTANTS = {
                         "return (int)((word >> (4 * (7 - n % 8))) & 15u);"),
     "wq4_scale_index": ("double s = dec(scales[(size_t)g * N + n]);",
                         "double s = dec(scales[(size_t)((g + 1) % (K / group)) * N + n]);"),
+    "dq8_drop_scale": ("(double)srow[n] * (double)qrow[n]", "(double)qrow[n]"),
+    "dq8_wrong_group": ("scales + (size_t)(k / group) * N;", "scales + (size_t)((k / group + 1) % (K / group)) * N;"),
+    "dq3_zero_sign": ("s * (double)wqo_code3(mat, N, k, n) - wqo_f16_to_double(zeros[n]);",
+                      "s * (double)wqo_code3(mat, N, k, n) + wqo_f16_to_double(zeros[n]);"),
+    "dq4_zero_sign": ("(double)(q - zp)", "(double)(q + zp)"),
+    "dq4_ignore_gidx": ("int grp = g_idx ? g_idx[k] : k / group;", "int grp = k / group;"),
     "w8a8_round_away": ("float rq = nearbyintf(r);", "float rq = roundf(r);"),
     "w8a8_scale_128": ("float sx = amax / 127.0f;", "float sx = amax / 128.0f;"),
     "w8a8_drop_term": ("        a[n] += p;\n", "        if (k > 0) a[n] += p;\n"),
