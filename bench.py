@@ -520,6 +520,124 @@ def run_w8a8(args, dev):
              "note": "exact int8 products on fp16 tcgen05 MMA; the int8 legacy mma.sync path measured 158 TOPS"}]
 
 
+def run_unfused(args, dev):
+    """The unfused baseline beside the fused kernels ("融合反量化与GEMM", 核心优化思路):
+    dequantize into a dense matrix in HBM, then a dense product (torch.matmul,
+    i.e. cuBLAS), against the fused call, for the three GEMVs and W4A16 at M = 1
+    and 16.  The packed weights rotate over enough copies to exceed the L2 three
+    times; the dense matrix is one scratch buffer, written and read every call."""
+    import torch
+
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    peak, peak_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.Stream(device=dev)
+    s = stream.cuda_stream
+    lines = []
+
+    def timed(issue, copies):
+        with torch.cuda.stream(stream):
+            for c in range(copies):
+                issue(c)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        per = max(copies, 4)
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+            for r in range(per):
+                issue(r % copies)
+        return _time_graph(graph, stream, 20, dev) / per * 1e3  # us per call
+
+    def case(name, packed, extra, dense_bytes, fused, dequant, product):
+        copies = max(2, -(-3 * l2 // max(packed, 1)))
+        state = [extra(c) for c in range(copies)]
+        f_us = timed(lambda c: fused(state[c]), copies)
+        d_us = timed(lambda c: dequant(state[c]), copies)
+        u_us = timed(lambda c: (dequant(state[c]), product(state[c])), copies)
+        fused_bytes = state[0]["alg_bytes"]
+        unfused_bytes = fused_bytes + 2 * dense_bytes
+        lines.append({"workload": name, "fused_us": f_us, "dequant_us": d_us, "unfused_us": u_us,
+                      "dense_product_us": u_us - d_us, "fused_speedup": u_us / f_us,
+                      "alg_bytes_fused": fused_bytes, "bytes_unfused": unfused_bytes,
+                      "traffic_saved_by_fusion": 1 - fused_bytes / unfused_bytes,
+                      "fused_GBps": fused_bytes / (f_us * 1e-6) / 1e9, "peak_GBps": peak, "peak_source": peak_kind,
+                      "dense_product": "torch.matmul (cuBLAS)", "copies": copies})
+
+    # W8: x fp32 [1, 4096], dense fp32 weights
+    d8 = syn.make_wq8(seed=1)
+    K, N = 4096, 4096
+    x8 = to_dev(d8["x"], dev)
+    y8 = torch.empty((1, N), dtype=torch.float32, device=dev)
+    W8 = torch.empty((K, N), dtype=torch.float32, device=dev)
+    b8 = alg_bytes_w8()
+
+    def e8(c):
+        return {"w": to_dev(d8["w"], dev), "s": to_dev(d8["scales"], dev), "alg_bytes": b8}
+    case("W8 g128 GEMV 4096x4096, M=1", K * N + (K // 128) * N * 4, e8, K * N * 4,
+         lambda t: wq.wq8_gemv(x8, t["w"], t["s"], y8, 1, K, N, 128, stream=s),
+         lambda t: wq.wq8_dequant(t["w"], t["s"], W8, K, N, 128, stream=s),
+         lambda t: torch.matmul(x8, W8, out=y8))
+
+    # W3: x fp16, dense fp16 weights
+    d3 = syn.make_wq3(seed=2)
+    x3 = to_dev(d3["x"], dev)
+    y3 = torch.empty((1, N), dtype=torch.float16, device=dev)
+    W3 = torch.empty((K, N), dtype=torch.float16, device=dev)
+    b3 = alg_bytes_w3()
+
+    def e3(c):
+        return {"m": to_dev(d3["mat"], dev), "s": to_dev(d3["scales"], dev), "z": to_dev(d3["zeros"], dev),
+                "alg_bytes": b3}
+    case("W3 per-column GEMV 4096x4096, M=1", 3 * K // 32 * N * 4, e3, K * N * 2,
+         lambda t: wq.wq3_gemv(x3, t["m"], t["s"], t["z"], y3, 1, K, N, stream=s),
+         lambda t: wq.wq3_dequant(t["m"], t["s"], t["z"], W3, K, N, stream=s),
+         lambda t: torch.matmul(x3, W3, out=y3))
+
+    # W4 act-order: fused = the sorted-rows GEMV of the decode step; dense fp16 weights
+    d4 = syn.make_wq4_actorder(seed=3)
+    N4 = 11008
+    x4 = to_dev(d4["x"], dev)
+    y4 = torch.empty((1, N4), dtype=torch.float16, device=dev)
+    W4 = torch.empty((K, N4), dtype=torch.float16, device=dev)
+    b4 = alg_bytes_w4g()
+
+    def e4(c):
+        t = {"qw": to_dev(d4["qweight"], dev), "s": to_dev(d4["scales"], dev), "z": to_dev(d4["qzeros"], dev),
+             "g": to_dev(d4["g_idx"], dev), "alg_bytes": b4}
+        t["qs"], t["perm"] = torch.empty_like(t["qw"]), torch.empty_like(t["g"])
+        wq.wq4_actorder_prepare(t["qw"], t["g"], K, N4, 128, t["qs"], t["perm"])
+        return t
+    case("W4 act-order g128 GEMV 4096x11008, M=1", K // 8 * N4 * 4 + (K // 128) * N4 * 3, e4, K * N4 * 2,
+         lambda t: wq.wq4_gemm_sorted(x4, t["qs"], t["s"], t["z"], t["perm"], y4, 1, K, N4, 128, wq.WQ_F16,
+                                      stream=s),
+         lambda t: wq.wq4_dequant(t["qw"], t["s"], t["z"], t["g"], W4, K, N4, 128, wq.WQ_F16, stream=s),
+         lambda t: torch.matmul(x4, W4, out=y4))
+
+    # W4A16 8192 x 28672, symmetric, bf16: M = 1 and M = 16
+    dw = syn.make_wq4_sym(seed=4, M=1, K=8192, N=28672, group=128)
+    Kw, Nw = 8192, 28672
+    Ww = torch.empty((Kw, Nw), dtype=torch.bfloat16, device=dev)
+    packed_w = Kw // 8 * Nw * 4 + (Kw // 128) * Nw * 2
+
+    def ew(c):
+        return {"qw": to_dev(dw["qweight"], dev), "s": to_dev(dw["scales"], dev), "alg_bytes": 0}
+    for M in (1, 16):
+        xw = to_dev(syn.f32_to_bf16_bits(syn.normal(4 + M, 1, (M, Kw))), dev)
+        yw = torch.empty((M, Nw), dtype=torch.bfloat16, device=dev)
+        bw = packed_w + M * Kw * 2 + M * Nw * 2
+
+        def ewm(c, bw=bw):
+            t = ew(c)
+            t["alg_bytes"] = bw
+            return t
+        case(f"W4A16 sym g128 8192x28672, M={M}", packed_w, ewm, Kw * Nw * 2,
+             lambda t, xw=xw, yw=yw, M=M: wq.wq4_gemm(xw, t["qw"], t["s"], None, None, yw, M, Kw, Nw, 128,
+                                                        wq.WQ_BF16, stream=s),
+             lambda t: wq.wq4_dequant(t["qw"], t["s"], None, None, Ww, Kw, Nw, 128, wq.WQ_BF16, stream=s),
+             lambda t, xw=xw, yw=yw: torch.matmul(xw, Ww, out=yw))
+    return lines
+
+
 # -------------------------------------------------------------------- main ----
 
 def main():
@@ -531,7 +649,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds of oracle work the reference arm aims for")
-    ap.add_argument("--workload", default="gemv_step", choices=["gemv_step", "wq4_sweep", "w8a8"],
+    ap.add_argument("--workload", default="gemv_step", choices=["gemv_step", "wq4_sweep", "w8a8", "unfused"],
                     help="gemv_step is the headline; the others print one extra line per case")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -549,7 +667,7 @@ def main():
     dev = torch.device(f"cuda:{local}")
     if args.workload != "gemv_step":
         torch.cuda.set_device(dev)
-        fn = run_wq4_sweep if args.workload == "wq4_sweep" else run_w8a8
+        fn = {"wq4_sweep": run_wq4_sweep, "w8a8": run_w8a8, "unfused": run_unfused}[args.workload]
         for ln in fn(args, dev):
             print(json.dumps(ln), flush=True)
         return

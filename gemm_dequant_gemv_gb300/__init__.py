@@ -32,6 +32,9 @@ SIGNATURES = {
     "wq4_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _U, _P]),
     "wq4_actorder_prepare": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "wq4_gemm_sorted": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _U, _P]),
+    "wq8_dequant": (_I, [_P, _P, _P, _I, _I, _I, _U, _P]),
+    "wq3_dequant": (_I, [_P, _P, _P, _P, _I, _I, _U, _P]),
+    "wq4_dequant": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _U, _P]),
     "w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _U, _P]),
     "w8a8_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
     "w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P]),
@@ -127,6 +130,21 @@ def wq4_gemm_sorted(x, qweight_sorted, scales, qzeros, perm, y, M, K, N, group_s
     _check("wq4_gemm_sorted", _lib.wq4_gemm_sorted(_ptr(x), _ptr(qweight_sorted), _ptr(scales), _ptr(qzeros),
                                                    _ptr(perm), _ptr(y), M, K, N, group_size, act_dtype, flags,
                                                    _stream(stream)))
+
+
+def wq8_dequant(w, scales, w_out, K, N, group_size, flags=0, stream=None):
+    _check("wq8_dequant", _lib.wq8_dequant(_ptr(w), _ptr(scales), _ptr(w_out), K, N, group_size, flags,
+                                           _stream(stream)))
+
+
+def wq3_dequant(mat, scales, zeros, w_out, K, N, flags=0, stream=None):
+    _check("wq3_dequant", _lib.wq3_dequant(_ptr(mat), _ptr(scales), _ptr(zeros), _ptr(w_out), K, N, flags,
+                                           _stream(stream)))
+
+
+def wq4_dequant(qweight, scales, qzeros, g_idx, w_out, K, N, group_size, act_dtype, flags=0, stream=None):
+    _check("wq4_dequant", _lib.wq4_dequant(_ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx), _ptr(w_out),
+                                           K, N, group_size, act_dtype, flags, _stream(stream)))
 
 
 def w8a8_gemm_workspace_bytes(M, K, N) -> int:

@@ -311,6 +311,38 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
   return from_cuda(launch_wq4_gemv(p, wmap, pmap, nullptr, a, act_dtype == WQ_BF16, qzeros != nullptr, true));
 }
 
+WQ_API wq_status wq8_dequant(const int8_t* w, const float* scales, float* w_out, int K, int N, int group_size,
+                             unsigned flags, void* stream) {
+  if (!w || !scales || !w_out) return WQ_ERR_NULL;
+  if (K < 1 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 16 || group_size % 16 != 0 || K % group_size != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(scales) || !aligned16(w_out)) return WQ_ERR_ALIGN;
+  return from_cuda(launch_wq8_dequant(w, scales, w_out, K, N, group_size, flags, static_cast<cudaStream_t>(stream)));
+}
+
+WQ_API wq_status wq3_dequant(const int32_t* mat, const void* scales, const void* zeros, void* w_out, int K, int N,
+                             unsigned flags, void* stream) {
+  if (!mat || !scales || !zeros || !w_out) return WQ_ERR_NULL;
+  if (K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 32 != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(mat) || !aligned16(scales) || !aligned16(zeros) || !aligned16(w_out)) return WQ_ERR_ALIGN;
+  return from_cuda(launch_wq3_dequant(mat, scales, zeros, w_out, K, N, flags, static_cast<cudaStream_t>(stream)));
+}
+
+WQ_API wq_status wq4_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                             const int32_t* g_idx, void* w_out, int K, int N, int group_size, int act_dtype,
+                             unsigned flags, void* stream) {
+  if (!qweight || !scales || !w_out) return WQ_ERR_NULL;
+  if (K < 32 || N < 1 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (group_size < 32 || group_size % 32 != 0 || K % group_size != 0 || N % 8 != 0) return WQ_ERR_SHAPE;
+  if (act_dtype != WQ_F16 && act_dtype != WQ_BF16) return WQ_ERR_UNSUPPORTED;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(w_out) || (qzeros && !aligned16(qzeros)) ||
+      (g_idx && !aligned16(g_idx)))
+    return WQ_ERR_ALIGN;
+  return from_cuda(launch_wq4_dequant(qweight, scales, qzeros, g_idx, w_out, K, N, group_size,
+                                      act_dtype == WQ_BF16, flags, static_cast<cudaStream_t>(stream)));
+}
+
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N) { return w8a8_workspace_bytes(M, K, N); }
 
 WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,

@@ -54,4 +54,13 @@ size_t wq4m_gemv_smem_bytes(int MT, int ng_max, int S, bool perm, int K);
 cudaError_t launch_wq4m_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                              const GemvArgs& a, int act_bf16, bool has_z, bool perm);
 
+// Standalone dequantization to a dense [K, N] matrix (wq_dequant.cu).
+cudaError_t launch_wq8_dequant(const int8_t* w, const float* scales, float* out, int K, int N, int group,
+                               unsigned flags, cudaStream_t stream);
+cudaError_t launch_wq3_dequant(const int32_t* mat, const void* scales, const void* zeros, void* out, int K, int N,
+                               unsigned flags, cudaStream_t stream);
+cudaError_t launch_wq4_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                               const int32_t* g_idx, void* out, int K, int N, int group, int act_bf16,
+                               unsigned flags, cudaStream_t stream);
+
 }  // namespace wq

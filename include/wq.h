@@ -179,6 +179,41 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
                                  int N, int group_size, int act_dtype, unsigned flags, void* stream);
 
 /*
+ * wq8_dequant / wq3_dequant / wq4_dequant -- standalone dequantization: the
+ * packed weights of wq8_gemv / wq3_gemv / wq4_gemm expanded into a dense
+ * row-major [K, N] matrix in device memory.  This is the separate-kernel path
+ * that fusion removes ("融合反量化与GEMM：LLM推理的CUDA内核优化实践",
+ * 核心优化思路 and CUDA内核架构: dequantize into a DRAM buffer, then a separate
+ * GEMM), kept as a baseline and for callers that want dense weights (for
+ * example to run a large-M product through a dense GEMM library).
+ *   wq8_dequant: w_out fp32 [K, N], w_out[k,n] = fp32(scales[k/g, n] * w[k,n])
+ *                (one rounding of the exact product).  Same shapes, group and
+ *                alignment rules as wq8_gemv.
+ *   wq3_dequant: w_out fp16 [K, N], w_out[k,n] = fp16(fp32 fma(s[n], q(k,n),
+ *                -zeros[n])): rounded once to fp32 and then to fp16, which is
+ *                the exact value rounded once whenever s[n]*q - zeros[n] fits
+ *                in 24 bits (always, for scales and zeros within a factor 2^10
+ *                of each other).  Same shape rules as wq3_gemv.
+ *   wq4_dequant: w_out [K, N] in act_dtype (fp16 or bf16),
+ *                w_out[k,n] = act(s[g(k), n] * (q(k,n) - z[g(k), n])), g(k) =
+ *                g_idx[k] (values outside [0, K/group) are clamped) or k/group,
+ *                z = 8 when qzeros is NULL: the product is exact in fp32 and
+ *                rounded once.  Same shape and alignment rules as wq4_gemm.
+ * All pointers are device pointers owned by the caller; w_out must not alias
+ * the inputs and must be 16-byte aligned.  Asynchronous on `stream`; flags may
+ * hold WQ_FLAG_PDL.  Errors: WQ_ERR_NULL, WQ_ERR_SHAPE, WQ_ERR_ALIGN,
+ * WQ_ERR_UNSUPPORTED (act_dtype), WQ_ERR_CUDA (launch failure); nothing runs
+ * on an argument error.
+ */
+WQ_API wq_status wq8_dequant(const int8_t* w, const float* scales, float* w_out, int K, int N,
+                             int group_size, unsigned flags, void* stream);
+WQ_API wq_status wq3_dequant(const int32_t* mat, const void* scales, const void* zeros,
+                             void* w_out, int K, int N, unsigned flags, void* stream);
+WQ_API wq_status wq4_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                             const int32_t* g_idx, void* w_out, int K, int N, int group_size,
+                             int act_dtype, unsigned flags, void* stream);
+
+/*
  * w8a8_gemm -- W8A8 dynamic-quantization GEMM.
  *   Sx[m]    = fp32(max_k |X[m,k]| / 127)              (fp32 division)
  *   Xq[m,k]  = clamp(rint(fp32(X[m,k] / Sx[m])), -127, 127)   (ties to even;

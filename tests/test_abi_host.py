@@ -112,6 +112,37 @@ def test_wq4_validation(wq):
     assert call(M=32, g=32, K=256) == wq.WQ_ERR_UNSUPPORTED  # the tensor-core path needs group % 64
 
 
+def test_dequant_validation(wq):
+    lib = wq.library()
+    f8, f3, f4 = lib.wq8_dequant, lib.wq3_dequant, lib.wq4_dequant
+    cases8 = [((0, A, A, 256, 256, 128, 0, 0), wq.WQ_ERR_NULL),
+              ((A, A, 0, 256, 256, 128, 0, 0), wq.WQ_ERR_NULL),
+              ((A, A, A, 200, 256, 128, 0, 0), wq.WQ_ERR_SHAPE),   # K % group
+              ((A, A, A, 256, 264, 128, 0, 0), wq.WQ_ERR_SHAPE),   # N % 16
+              ((A, A, A, 256, 256, 24, 0, 0), wq.WQ_ERR_SHAPE),    # group % 16
+              ((A, A, MIS, 256, 256, 128, 0, 0), wq.WQ_ERR_ALIGN)]
+    for args, want in cases8:
+        assert f8(*args) == want, args
+    cases3 = [((A, A, 0, A, 64, 64, 0, 0), wq.WQ_ERR_NULL),
+              ((A, A, A, A, 48, 64, 0, 0), wq.WQ_ERR_SHAPE),       # K % 32
+              ((A, A, A, A, 64, 60, 0, 0), wq.WQ_ERR_SHAPE),       # N % 8
+              ((A, A, A, MIS, 64, 64, 0, 0), wq.WQ_ERR_ALIGN)]
+    for args, want in cases3:
+        assert f3(*args) == want, args
+    ok4 = [A, A, None, None, A, 256, 256, 128, wq.WQ_F16, 0, 0]
+    cases4 = [({0: 0}, wq.WQ_ERR_NULL), ({4: 0}, wq.WQ_ERR_NULL),
+              ({7: 48}, wq.WQ_ERR_SHAPE),                            # group % 32
+              ({5: 320}, wq.WQ_ERR_SHAPE),                           # K % group
+              ({6: 260}, wq.WQ_ERR_SHAPE),                           # N % 8
+              ({8: 0}, wq.WQ_ERR_UNSUPPORTED),                       # not fp16 / bf16
+              ({2: MIS}, wq.WQ_ERR_ALIGN), ({3: MIS}, wq.WQ_ERR_ALIGN), ({4: MIS}, wq.WQ_ERR_ALIGN)]
+    for edits, want in cases4:
+        a = list(ok4)
+        for i, v in edits.items():
+            a[i] = v
+        assert f4(*a) == want, edits
+
+
 def test_w8a8_validation(wq):
     f = wq.library().w8a8_gemm
     need = wq.w8a8_gemm_workspace_bytes(64, 128, 64)
