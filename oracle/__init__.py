@@ -94,6 +94,8 @@ def _bind(lib):
     lib.wqo_wq4_dequant.argtypes = [I, P, P, P, P, I, I, I, P]
     lib.wqo_w8a8_quant_rows.restype = None
     lib.wqo_w8a8_quant_rows.argtypes = [P, I, I, P, P]
+    lib.wqo_w8a8_quant_rows_smooth.restype = None
+    lib.wqo_w8a8_quant_rows_smooth.argtypes = [P, P, I, I, P, P]
     lib.wqo_w8a8_gemm_rows.restype = I
     lib.wqo_w8a8_gemm_rows.argtypes = [P, P, P, P, I, I, I, P, I, P, P, P]
     return lib
@@ -286,6 +288,16 @@ def w8a8_quant_rows(X_bits):
     M, K = X.shape
     Xq = np.empty((M, K), dtype=np.int8); Sx = np.empty((M,), dtype=np.float32)
     _load().wqo_w8a8_quant_rows(_ptr(X), M, K, _ptr(Xq), _ptr(Sx))
+    return Xq, Sx
+
+
+def w8a8_quant_rows_smooth(X_bits, smooth):
+    """Smoothquant's activation side: X / smooth per channel (fp32), then per-row quantization."""
+    X = _c(X_bits, np.uint16); s = _c(smooth, np.float32)
+    M, K = X.shape
+    assert s.shape == (K,)
+    Xq = np.empty((M, K), dtype=np.int8); Sx = np.empty((M,), dtype=np.float32)
+    _load().wqo_w8a8_quant_rows_smooth(_ptr(X), _ptr(s), M, K, _ptr(Xq), _ptr(Sx))
     return Xq, Sx
 
 

@@ -295,6 +295,32 @@ void wqo_w8a8_quant_rows(const uint16_t* X, int M, int K, int8_t* Xq, float* Sx)
   }
 }
 
+void wqo_w8a8_quant_rows_smooth(const uint16_t* X, const float* smooth, int M, int K, int8_t* Xq,
+                                float* Sx) {
+  /* [QC] Smoothquant: Y = (X diag(s)^-1) . (diag(s) W): every activation is
+   * divided by its channel's s (one correctly rounded fp32 division), then the
+   * row is quantized exactly as in wqo_w8a8_quant_rows. */
+  float* xs = (float*)malloc((size_t)K * sizeof(float));
+  for (int m = 0; m < M; ++m) {
+    float peak = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) / smooth[k];
+      if (fabsf(xs[k]) > peak) peak = fabsf(xs[k]);
+    }
+    const float scale = peak / 127.0f;         /* fp32 division */
+    Sx[m] = scale;
+    for (int k = 0; k < K; ++k) {
+      float code = 0.0f;
+      if (scale != 0.0f) {
+        code = nearbyintf(xs[k] / scale);      /* round half to even */
+        code = code > 127.0f ? 127.0f : (code < -127.0f ? -127.0f : code);
+      }
+      Xq[(size_t)m * K + k] = (int8_t)(int)code;
+    }
+  }
+  free(xs);
+}
+
 int wqo_w8a8_gemm_rows(const int8_t* Xq, const float* Sx, const int8_t* W,
                        const float* Sw, int M, int K, int N,
                        const int32_t* rows, int nrows,

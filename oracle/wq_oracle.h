@@ -100,6 +100,12 @@ void wqo_w8a8_quant_rows(const uint16_t* X, int M, int K, int8_t* Xq, float* Sx)
  *   y[r, n]   = Sx[m] * acc[r, n] * Sw[n]          (double, before rounding)
  *   abs_sum   = sum_k |Sx[m] Xq[m,k] * Sw[n] W[k,n]|
  * Returns 0 if every acc fits int32, else 1. */
+/* Smoothquant's run-time half: X'[m,k] = fp32(X[m,k] / smooth[k]), then the
+ * per-row quantization of wqo_w8a8_quant_rows applied to X' (the weights are
+ * the caller's int8 codes of diag(s) W, prepared offline). */
+void wqo_w8a8_quant_rows_smooth(const uint16_t* X, const float* smooth, int M, int K, int8_t* Xq,
+                                float* Sx);
+
 int wqo_w8a8_gemm_rows(const int8_t* Xq, const float* Sx, const int8_t* W,
                        const float* Sw, int M, int K, int N,
                        const int32_t* rows, int nrows,

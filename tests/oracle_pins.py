@@ -274,6 +274,33 @@ def pin_wq4_invariants():
     assert np.allclose(yb16, ref, rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------------------------- smoothquant ----
+
+def pin_w8a8_smooth():
+    """Smoothquant's activation division: s = 1 is the plain quantizer bit for bit;
+    powers of two scale X exactly, so the result is the plain quantizer applied to
+    X * 2^-e (numpy, exact in bf16); an outlier channel divided by a large s no
+    longer sets the row scale."""
+    r = _rng(23)
+    M, K = 6, 256
+    Xf = r.normal(0, 1, (M, K)).astype(np.float32)
+    Xf[:, 17] = np.where(np.arange(M) % 2 == 0, 100.0, -100.0)  # an outlier channel
+    X = syn.f32_to_bf16_bits(Xf)
+    Xq0, Sx0 = oracle.w8a8_quant_rows(X)
+    Xq1, Sx1 = oracle.w8a8_quant_rows_smooth(X, np.ones(K, np.float32))
+    assert np.array_equal(Xq0, Xq1) and np.array_equal(Sx0.view(np.uint32), Sx1.view(np.uint32))
+    e = r.integers(-3, 4, K)
+    s = (2.0 ** e).astype(np.float32)
+    Xs = syn.f32_to_bf16_bits(syn.bf16_bits_to_f32(X) / s)   # exact: a power-of-two rescale
+    Xq2, Sx2 = oracle.w8a8_quant_rows(Xs)
+    Xq3, Sx3 = oracle.w8a8_quant_rows_smooth(X, s)
+    assert np.array_equal(Xq2, Xq3) and np.array_equal(Sx2.view(np.uint32), Sx3.view(np.uint32))
+    s_out = np.ones(K, np.float32)
+    s_out[17] = 64.0
+    _, Sx4 = oracle.w8a8_quant_rows_smooth(X, s_out)
+    assert np.all(Sx4 < Sx0), (Sx4, Sx0)
+
+
 # ----------------------------------------------------------- dequantization ----
 
 def pin_dequant_hand():

@@ -39,6 +39,10 @@ MUTANTS = {
                       "s * (double)wqo_code3(mat, N, k, n) + wqo_f16_to_double(zeros[n]);"),
     "dq4_zero_sign": ("(double)(q - zp)", "(double)(q + zp)"),
     "dq4_ignore_gidx": ("int grp = g_idx ? g_idx[k] : k / group;", "int grp = k / group;"),
+    "smooth_multiply": ("xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) / smooth[k];",
+                        "xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) * smooth[k];"),
+    "smooth_ignored": ("xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) / smooth[k];",
+                       "xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]);"),
     "w8a8_round_away": ("float rq = nearbyintf(r);", "float rq = roundf(r);"),
     "w8a8_scale_128": ("float sx = amax / 127.0f;", "float sx = amax / 128.0f;"),
     "w8a8_drop_term": ("        a[n] += p;\n", "        if (k > 0) a[n] += p;\n"),
