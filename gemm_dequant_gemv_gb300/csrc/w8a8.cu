@@ -46,7 +46,12 @@ int device_max_smem();
 namespace {
 
 // ------------------------------------------------------------ quantization --
+// smooth (fp32 [K] or null): Smoothquant's per-channel divisor ("Quantization
+// CUDA", Smoothquant: Y = (X diag(s)^-1)(diag(s) W)); every activation is
+// divided by it (one correctly rounded fp32 division) before the row amax and
+// the codes.
 __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restrict__ X, int K,
+                                                         const float* __restrict__ smooth,
                                                          __half* __restrict__ xq16, float* __restrict__ sx_ws,
                                                          int8_t* __restrict__ xq_out, float* __restrict__ sx_out) {
   __shared__ float red[8];
@@ -54,14 +59,25 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
   pdl_wait();
   const uint16_t* row = X + size_t(m) * K;
   float amax = 0.f;
-  for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
+  // the 8 activations k .. k+7 of this row, divided by the smoothing factors if any
+  auto load8 = [&](int k, float (&x)[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(row + k);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] & 0xFFFFu)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] >> 16)));
+    for (int i = 0; i < 8; ++i) x[i] = bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+    if (smooth) {
+      const float4 s0 = *reinterpret_cast<const float4*>(smooth + k);
+      const float4 s1 = *reinterpret_cast<const float4*>(smooth + k + 4);
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __fdiv_rn(x[i], sv[i]);
     }
+  };
+  for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
+    float x[8];
+    load8(k, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -72,14 +88,13 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const float sx = __fdiv_rn(amax, 127.0f);
   for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + k);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
+    load8(k, x);
     int q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float x = bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
       int c = 0;
-      if (sx != 0.f) c = min(127, max(-127, __float2int_rn(__fdiv_rn(x, sx))));
+      if (sx != 0.f) c = min(127, max(-127, __float2int_rn(__fdiv_rn(x[i], sx))));
       q[i] = c;
     }
     // fp16 copies in the GEMM's operand order: k0 + {0,2}, {4,6}, {1,3}, {5,7}
@@ -423,7 +438,7 @@ size_t w8a8_workspace_bytes(int M, int K, int N) {
 
 cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
                         int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const float* smooth) {
   const SmemW8A8 L;
   if (L.total > static_cast<size_t>(device_max_smem())) return cudaErrorNotSupported;
   __half* xq16 = static_cast<__half*>(workspace);
@@ -432,7 +447,7 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
   // 1) per-row quantization
   {
     const uint16_t* Xp = static_cast<const uint16_t*>(X);
-    void* args[] = {&Xp, &K, &xq16, &sx, &Xq_out, &Sx_out};
+    void* args[] = {&Xp, &K, &smooth, &xq16, &sx, &Xq_out, &Sx_out};
     cudaError_t e = launch_ex(reinterpret_cast<const void*>(w8a8_quant_kernel), dim3(M), dim3(256), 0, flags, stream,
                               args);
     if (e != cudaSuccess) return e;

@@ -360,4 +360,21 @@ WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void
                                static_cast<cudaStream_t>(stream)));
 }
 
+WQ_API wq_status w8a8_gemm_smooth(const void* X, const float* smooth, const int8_t* W, const float* Sw, void* Y,
+                                  int M, int K, int N, int8_t* Xq_out, float* Sx_out, int32_t* acc_out,
+                                  void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  if (!smooth) return WQ_ERR_NULL;
+  if (!aligned16(smooth)) return WQ_ERR_ALIGN;
+  if (!X || !W || !Sw || !Y || !workspace) return (!workspace && X && W && Sw && Y) ? WQ_ERR_WORKSPACE : WQ_ERR_NULL;
+  if (M < 1 || K < 64 || N < 16 || M > kMaxDim || K > 65536 || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 64 != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Sw) || !aligned16(Y) || (Xq_out && !aligned16(Xq_out)) ||
+      (Sx_out && !aligned16(Sx_out)) || (acc_out && !aligned16(acc_out)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return WQ_ERR_ALIGN;
+  if (workspace_bytes < w8a8_workspace_bytes(M, K, N)) return WQ_ERR_WORKSPACE;
+  return from_cuda(launch_w8a8(X, W, Sw, Y, M, K, N, Xq_out, Sx_out, acc_out, workspace, flags,
+                               static_cast<cudaStream_t>(stream), smooth));
+}
+
 }  // extern "C"

@@ -15,9 +15,10 @@ cudaError_t launch_wq4_mma(const void* x, const int32_t* qweight, const void* sc
 
 size_t w8a8_workspace_bytes(int M, int K, int N);
 
+// smooth: Smoothquant's per-channel divisor of the activations (fp32 [K]), or null.
 cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
                         int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const float* smooth = nullptr);
 
 // Act-order preparation (host-driven, synchronous on `stream`): 0 = ok,
 // 1 = g_idx is not a grouping with exactly `group` rows per group, 2 = CUDA error.

@@ -235,6 +235,24 @@ WQ_API wq_status w8a8_gemm(const void* X, const int8_t* W, const float* Sw, void
                            int32_t* acc_out, void* workspace, size_t workspace_bytes,
                            unsigned flags, void* stream);
 
+/*
+ * w8a8_gemm_smooth -- w8a8_gemm with Smoothquant's activation side
+ * ([QC] Smoothquant: Y = (X diag(s)^-1) . (diag(s) W), which moves the
+ * quantization difficulty of outlier activation channels onto the weights):
+ *   X'[m,k] = fp32(X[m,k] / smooth[k])     (one correctly rounded division)
+ * and then everything w8a8_gemm does, on X' instead of X (Sx, Xq_out and
+ * Sx_out describe X').  The caller supplies W as the int8 codes of diag(s) W
+ * with their per-column Sw, prepared offline.
+ *   smooth fp32 [K], device, 16-byte aligned; every entry finite and > 0 (not
+ *   checked: it is device data; other values give meaningless codes).
+ *   Everything else as in w8a8_gemm (same errors; smooth NULL is WQ_ERR_NULL).
+ */
+WQ_API wq_status w8a8_gemm_smooth(const void* X, const float* smooth, const int8_t* W,
+                                  const float* Sw, void* Y, int M, int K, int N,
+                                  int8_t* Xq_out, float* Sx_out, int32_t* acc_out,
+                                  void* workspace, size_t workspace_bytes, unsigned flags,
+                                  void* stream);
+
 /* Bytes of device workspace w8a8_gemm needs for this shape (0 on bad shape). */
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
 

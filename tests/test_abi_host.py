@@ -143,6 +143,17 @@ def test_dequant_validation(wq):
         assert f4(*a) == want, edits
 
 
+def test_w8a8_smooth_validation(wq):
+    f = wq.library().w8a8_gemm_smooth
+    ok = [A, A, A, A, A, 128, 256, 256, None, None, None, A, 1 << 20, 0, 0]
+    for edits, want in (({1: 0}, wq.WQ_ERR_NULL), ({1: MIS}, wq.WQ_ERR_ALIGN), ({0: 0}, wq.WQ_ERR_NULL),
+                        ({6: 96}, wq.WQ_ERR_SHAPE), ({7: 40}, wq.WQ_ERR_SHAPE), ({12: 16}, wq.WQ_ERR_WORKSPACE)):
+        a = list(ok)
+        for i, v in edits.items():
+            a[i] = v
+        assert f(*a) == want, edits
+
+
 def test_w8a8_validation(wq):
     f = wq.library().w8a8_gemm
     need = wq.w8a8_gemm_workspace_bytes(64, 128, 64)

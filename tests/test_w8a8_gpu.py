@@ -90,3 +90,44 @@ def test_w8a8_repeat_bit_identical(G):
     y1 = G.bits_u16(run_w8a8(G, d["X"], d["W"], d["Sw"], want_acc=False)[0])
     y2 = G.bits_u16(run_w8a8(G, d["X"], d["W"], d["Sw"], want_acc=False)[0])
     assert np.array_equal(y1, y2)
+
+
+def test_w8a8_smooth_parity(G):
+    """Smoothquant: X / s per channel before the row quantization; the weights are the
+    int8 codes of diag(s) W.  Sx, Xq and the int32 product bit-exact, Y under the bar."""
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    import oracle
+    import synthetic as syn
+    from tolerance import U_BF16, within
+    M, K, N = 200, 512, 272
+    r = np.random.default_rng(31)
+    Xf = r.normal(0, 1, (M, K)).astype(np.float32)
+    Xf[:, [5, 77, 300]] *= 30.0                              # outlier channels
+    X_bits = syn.f32_to_bf16_bits(Xf)
+    amax_c = np.abs(syn.bf16_bits_to_f32(X_bits)).max(axis=0)
+    smooth = np.sqrt(np.maximum(amax_c, 1e-3)).astype(np.float32)   # s = sqrt(max|X[:, k]|)
+    Wf = r.normal(0, 0.02, (K, N)).astype(np.float32) * smooth[:, None]   # diag(s) W
+    Sw = (np.abs(Wf).max(axis=0) / np.float32(127.0)).astype(np.float32)
+    Wq = np.clip(np.rint(Wf / Sw[None, :]), -127, 127).astype(np.int8)
+    X, Wd, Swd, sd = G.dev(X_bits), G.dev(Wq), G.dev(Sw), G.dev(smooth)
+    buf, Y = G.guarded((M, N), torch.bfloat16)
+    Xq = torch.empty((M, K), dtype=torch.int8, device=G.DEV)
+    Sx = torch.empty((M,), dtype=torch.float32, device=G.DEV)
+    acc = torch.empty((M, N), dtype=torch.int32, device=G.DEV)
+    nb = wq.w8a8_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(nb, dtype=torch.uint8, device=G.DEV)
+    wq.w8a8_gemm_smooth(X, sd, Wd, Swd, Y, M, K, N, Xq, Sx, acc, ws, nb)
+    torch.cuda.synchronize()
+    G.check_canary(buf, M * N)
+    Xq_ref, Sx_ref = oracle.w8a8_quant_rows_smooth(X_bits, smooth)
+    assert np.array_equal(Sx.cpu().numpy().view(np.uint32), Sx_ref.view(np.uint32)), "Sx differs"
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref), "Xq differs"
+    acc_ref, y_ref, a, ovf = oracle.w8a8_gemm_rows(Xq_ref, Sx_ref, Wq, Sw)
+    assert not ovf
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), acc_ref), "int32 accumulator differs"
+    ok, worst = within(G.to_f64(Y), y_ref, a, U_BF16)
+    assert ok, f"max |err|/bound = {worst:.3g}"
+    # smoothing lowers the row scales that the outlier channels set
+    _, Sx_plain = oracle.w8a8_quant_rows(X_bits)
+    assert np.all(Sx_ref <= Sx_plain) and np.mean(Sx_ref) < 0.5 * np.mean(Sx_plain)
