@@ -96,6 +96,10 @@ def _bind(lib):
     lib.wqo_w8a8_quant_rows.argtypes = [P, I, I, P, P]
     lib.wqo_w8a8_quant_rows_smooth.restype = None
     lib.wqo_w8a8_quant_rows_smooth.argtypes = [P, P, I, I, P, P]
+    lib.wqo_w8a8_outlier_columns.restype = None
+    lib.wqo_w8a8_outlier_columns.argtypes = [P, I, I, ctypes.c_float, P]
+    lib.wqo_w8a8_outlier_rows.restype = I
+    lib.wqo_w8a8_outlier_rows.argtypes = [P, P, P, P, P, P, I, I, I, P, I, P, P, P]
     lib.wqo_w8a8_gemm_rows.restype = I
     lib.wqo_w8a8_gemm_rows.argtypes = [P, P, P, P, I, I, I, P, I, P, P, P]
     return lib
@@ -316,6 +320,29 @@ def w8a8_gemm_rows(Xq, Sx, W, Sw, rows=None):
     ovf = _load().wqo_w8a8_gemm_rows(_ptr(Xq), _ptr(Sx), _ptr(W), _ptr(Sw), M, K, N, _ptr(r), nr,
                                      _ptr(acc), _ptr(y), _ptr(a))
     return acc, y, a, bool(ovf)
+
+
+def w8a8_outlier(X_bits, W, Sw, threshold, rows=None):
+    """LLM.int8(): (is_outlier, Xq, Sx, acc, y, abs_sum, overflow).  Columns with some
+    |x| > threshold go through the 16-bit part; Xq / Sx quantize X with those
+    columns set to zero."""
+    X = _c(X_bits, np.uint16); W = _c(W, np.int8); Sw = _c(Sw, np.float32)
+    M, K = X.shape
+    K2, N = W.shape
+    assert K2 == K and Sw.shape == (N,)
+    flags = np.empty((K,), dtype=np.uint8)
+    _load().wqo_w8a8_outlier_columns(_ptr(X), M, K, float(threshold), _ptr(flags))
+    Xm = X.copy()
+    Xm[:, flags.astype(bool)] = 0          # bf16 +0: the regular part only
+    Xq, Sx = w8a8_quant_rows(Xm)
+    if rows is None:
+        r, nr = None, M
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32)); nr = int(r.size)
+    acc = np.empty((nr, N), dtype=np.int64); y = np.empty((nr, N)); a = np.empty((nr, N))
+    ovf = _load().wqo_w8a8_outlier_rows(_ptr(X), _ptr(flags), _ptr(Xq), _ptr(Sx), _ptr(W), _ptr(Sw), M, K, N,
+                                        _ptr(r), nr, _ptr(acc), _ptr(y), _ptr(a))
+    return flags.astype(bool), Xq, Sx, acc, y, a, bool(ovf)
 
 
 def w8a8_gemm(X_bits, W, Sw, rows=None):

@@ -353,3 +353,42 @@ int wqo_w8a8_gemm_rows(const int8_t* Xq, const float* Sx, const int8_t* W,
   free(absacc);
   return overflow;
 }
+
+/* ------------------------------------------------------------------------ */
+/* LLM.int8() mixed-precision decomposition ([QC] LLM.int8(): the activation */
+/* columns holding a value above the threshold, with the matching weight     */
+/* rows, are multiplied in 16-bit floating point; the rest in int8; the two  */
+/* results are added).                                                      */
+/* ------------------------------------------------------------------------ */
+
+void wqo_w8a8_outlier_columns(const uint16_t* X, int M, int K, float threshold, uint8_t* is_outlier) {
+  for (int k = 0; k < K; ++k) {
+    is_outlier[k] = 0;
+    for (int m = 0; m < M; ++m)
+      if (fabs(wqo_bf16_to_double(X[(size_t)m * K + k])) > (double)threshold) is_outlier[k] = 1;
+  }
+}
+
+int wqo_w8a8_outlier_rows(const uint16_t* X, const uint8_t* is_outlier, const int8_t* Xq,
+                          const float* Sx, const int8_t* W, const float* Sw, int M, int K, int N,
+                          const int32_t* rows, int nrows, int64_t* acc, double* y, double* abs_sum) {
+  /* int8 part: the regular columns (their codes; outlier columns have code 0),
+   * exactly as wqo_w8a8_gemm_rows; 16-bit part: x[m,k] * Sw[n] * W[k,n] over
+   * the outlier columns, with the activation as stored and the weight row
+   * dequantized. */
+  int overflow = wqo_w8a8_gemm_rows(Xq, Sx, W, Sw, M, K, N, rows, nrows, acc, y, abs_sum);
+  for (int r = 0; r < nrows; ++r) {
+    int m = rows ? rows[r] : r;
+    for (int k = 0; k < K; ++k) {
+      if (!is_outlier[k]) continue;
+      double xv = wqo_bf16_to_double(X[(size_t)m * K + k]);
+      for (int n = 0; n < N; ++n) {
+        double t = xv * ((double)Sw[n] * (double)W[(size_t)k * N + n]);
+        y[(size_t)r * N + n] += t;
+        abs_sum[(size_t)r * N + n] += fabs(t);
+      }
+    }
+  }
+  return overflow;
+}
+

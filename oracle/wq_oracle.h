@@ -111,6 +111,18 @@ int wqo_w8a8_gemm_rows(const int8_t* Xq, const float* Sx, const int8_t* W,
                        const int32_t* rows, int nrows,
                        int64_t* acc, double* y, double* abs_sum);
 
+/* LLM.int8() decomposition: is_outlier[k] = 1 when some |X[m,k]| > threshold
+ * (strictly greater).  wqo_w8a8_outlier_rows takes Xq / Sx of X with the
+ * outlier columns set to zero (the regular part) and returns
+ *   y[m,n] = Sx[m] * sum_k Xq[m,k] W[k,n] * Sw[n]
+ *          + sum_{k outlier} X[m,k] * (Sw[n] * W[k,n])
+ * with acc the int8 part's exact sum and abs_sum the magnitude sum of both
+ * parts; the return value is 1 if an int8 sum leaves int32. */
+void wqo_w8a8_outlier_columns(const uint16_t* X, int M, int K, float threshold, uint8_t* is_outlier);
+int wqo_w8a8_outlier_rows(const uint16_t* X, const uint8_t* is_outlier, const int8_t* Xq,
+                          const float* Sx, const int8_t* W, const float* Sw, int M, int K, int N,
+                          const int32_t* rows, int nrows, int64_t* acc, double* y, double* abs_sum);
+
 #ifdef __cplusplus
 }
 #endif

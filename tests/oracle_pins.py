@@ -301,6 +301,40 @@ def pin_w8a8_smooth():
     assert np.all(Sx4 < Sx0), (Sx4, Sx0)
 
 
+# ------------------------------------------------------------------ LLM.int8() ----
+
+def pin_w8a8_outlier():
+    """LLM.int8(): no column above the threshold is the plain W8A8 path bit for bit;
+    every column above it is the 16-bit product X . (Sw W) (numpy float64); a value
+    equal to the threshold is not an outlier (strictly greater); in general the
+    result is the plain path on X with the outlier columns zeroed plus the
+    16-bit product over those columns (numpy)."""
+    r = _rng(29)
+    M, K, N = 5, 128, 24
+    Xf = r.normal(0, 1, (M, K)).astype(np.float32)
+    Xf[2, 9] = 6.0                         # equal to the threshold: regular
+    Xf[1, 40] = -7.5                       # above it: column 40 is an outlier
+    Xf[3, 100] = 12.0                      # column 100 too
+    X = syn.f32_to_bf16_bits(Xf)
+    W = r.integers(-127, 128, (K, N), dtype=np.int8)
+    Sw = r.uniform(0.001, 0.01, N).astype(np.float32)
+    xv = syn.bf16_bits_to_f32(X).astype(np.float64)
+    wv = W.astype(np.float64) * Sw.astype(np.float64)[None, :]
+    flags, Xq, Sx, acc, y, a, ovf = oracle.w8a8_outlier(X, W, Sw, np.inf)
+    Xq0, Sx0, acc0, y0, a0, _ = oracle.w8a8_gemm(X, W, Sw)
+    assert not flags.any() and np.array_equal(Xq, Xq0) and np.array_equal(acc, acc0) and np.array_equal(y, y0)
+    flags, Xq, Sx, acc, y, a, ovf = oracle.w8a8_outlier(X, W, Sw, -1.0)
+    assert flags.all() and not Xq.any() and not acc.any()
+    assert np.allclose(y, xv @ wv, rtol=1e-12, atol=1e-15)
+    flags, Xq, Sx, acc, y, a, ovf = oracle.w8a8_outlier(X, W, Sw, 6.0)
+    assert sorted(np.nonzero(flags)[0].tolist()) == [40, 100], np.nonzero(flags)
+    Xm = X.copy()
+    Xm[:, [40, 100]] = 0
+    _, _, acc_m, y_m, _, _ = oracle.w8a8_gemm(Xm, W, Sw)
+    assert np.array_equal(acc, acc_m)
+    assert np.allclose(y, y_m + xv[:, [40, 100]] @ wv[[40, 100]], rtol=1e-12, atol=1e-15)
+
+
 # ----------------------------------------------------------- dequantization ----
 
 def pin_dequant_hand():

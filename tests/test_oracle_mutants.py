@@ -43,6 +43,11 @@ MUTANTS = {
                         "xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) * smooth[k];"),
     "smooth_ignored": ("xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]) / smooth[k];",
                        "xs[k] = (float)wqo_bf16_to_double(X[(size_t)m * K + k]);"),
+    "outlier_ge": ("if (fabs(wqo_bf16_to_double(X[(size_t)m * K + k])) > (double)threshold) is_outlier[k] = 1;",
+                   "if (fabs(wqo_bf16_to_double(X[(size_t)m * K + k])) >= (double)threshold) is_outlier[k] = 1;"),
+    "outlier_sign": ("        y[(size_t)r * N + n] += t;\n", "        y[(size_t)r * N + n] -= t;\n"),
+    "outlier_drop_sw": ("double t = xv * ((double)Sw[n] * (double)W[(size_t)k * N + n]);",
+                        "double t = xv * (double)W[(size_t)k * N + n];"),
     "w8a8_round_away": ("float rq = nearbyintf(r);", "float rq = roundf(r);"),
     "w8a8_scale_128": ("float sx = amax / 127.0f;", "float sx = amax / 128.0f;"),
     "w8a8_drop_term": ("        a[n] += p;\n", "        if (k > 0) a[n] += p;\n"),
