@@ -515,9 +515,48 @@ def run_w8a8(args, dev):
     ms = _time_graph(graph, stream, max(3, args.steps // 400), dev) / per
     pk, pk_kind = measured_bf16_peak()
     tf = 2 * M * K * N / (ms * 1e-3) / 1e12
-    return [{"workload": f"W8A8 dynamic quant GEMM M={M} K={K} N={N}", "us_per_call": ms * 1e3, "tops": tf,
-             "peak_tflops_f16_dense": pk, "peak_source": pk_kind, "frac_of_tensor_peak": tf / pk,
-             "note": "exact int8 products on fp16 tcgen05 MMA; the int8 legacy mma.sync path measured 158 TOPS"}]
+    lines = [{"workload": f"W8A8 dynamic quant GEMM M={M} K={K} N={N}", "us_per_call": ms * 1e3, "tops": tf,
+              "peak_tflops_f16_dense": pk, "peak_source": pk_kind, "frac_of_tensor_peak": tf / pk,
+              "note": "exact int8 products on fp16 tcgen05 MMA; the int8 legacy mma.sync path measured 158 TOPS"}]
+
+    # the two variants on the same shape: LLM.int8() with 8 outlier columns (0.1 % of K,
+    # values 8..15 in one row each, threshold 6) and Smoothquant with s = sqrt(max_m |X[m,k]|)
+    import numpy as np
+    Xo = d["X"].copy()
+    r = np.random.default_rng(5)
+    cols = r.choice(K, size=8, replace=False)
+    for i, c in enumerate(cols):
+        Xo[r.integers(0, M), c] = syn.f32_to_bf16_bits(np.array([8.0 + i], np.float32))[0]
+    Xo_d = to_dev(Xo, dev)
+    nbo = wq.w8a8_gemm_outlier_workspace_bytes(M, K, N)
+    wso = torch.empty(nbo, dtype=torch.uint8, device=dev)
+    nout = torch.zeros((4,), dtype=torch.int32, device=dev)
+
+    def outlier(flags):
+        wq.w8a8_gemm_outlier(Xo_d, W, Sw, Y, M, K, N, 6.0, n_outliers_out=nout, workspace=wso, workspace_bytes=nbo,
+                             flags=flags, stream=stream)
+    smooth = to_dev(np.sqrt(np.maximum(np.abs(syn.bf16_bits_to_f32(d["X"])).max(axis=0), 1e-3)).astype(np.float32),
+                    dev)
+
+    def smoothed(flags):
+        wq.w8a8_gemm_smooth(X, smooth, W, Sw, Y, M, K, N, workspace=ws, workspace_bytes=nbytes, flags=flags,
+                            stream=stream)
+    for name, fn in (("LLM.int8() decomposition, 8 outlier columns, threshold 6", outlier),
+                     ("Smoothquant activation smoothing", smoothed)):
+        with torch.cuda.stream(stream):
+            fn(0)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for _ in range(per):
+                fn(wq.WQ_FLAG_PDL)
+        msv = _time_graph(g, stream, max(3, args.steps // 400), dev) / per
+        line = {"workload": f"W8A8 M={M} K={K} N={N}, {name}", "us_per_call": msv * 1e3,
+                "overhead_vs_plain": msv / ms - 1, "tops": 2 * M * K * N / (msv * 1e-3) / 1e12}
+        if fn is outlier:
+            line["outlier_columns"] = int(nout[0])
+        lines.append(line)
+    return lines
 
 
 def run_unfused(args, dev):

@@ -37,6 +37,8 @@ SIGNATURES = {
     "wq4_dequant": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _U, _P]),
     "w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _U, _P]),
     "w8a8_gemm_smooth": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _U, _P]),
+    "w8a8_gemm_outlier": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P, _P, _P, _SZ, _U, _P]),
+    "w8a8_gemm_outlier_workspace_bytes": (_SZ, [_I, _I, _I]),
     "w8a8_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
     "w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P]),
     "w8a8_gemm_noalloc_max_scratch_bytes": (_SZ, []),
@@ -164,6 +166,18 @@ def w8a8_gemm_smooth(X, smooth, W, Sw, Y, M, K, N, Xq_out=None, Sx_out=None, acc
     _check("w8a8_gemm_smooth", _lib.w8a8_gemm_smooth(_ptr(X), _ptr(smooth), _ptr(W), _ptr(Sw), _ptr(Y), M, K, N,
                                                      _ptr(Xq_out), _ptr(Sx_out), _ptr(acc_out), _ptr(workspace),
                                                      workspace_bytes, flags, _stream(stream)))
+
+
+def w8a8_gemm_outlier_workspace_bytes(M, K, N) -> int:
+    return int(_lib.w8a8_gemm_outlier_workspace_bytes(M, K, N))
+
+
+def w8a8_gemm_outlier(X, W, Sw, Y, M, K, N, threshold=6.0, Xq_out=None, Sx_out=None, acc_out=None,
+                      n_outliers_out=None, workspace=None, workspace_bytes=0, flags=0, stream=None):
+    _check("w8a8_gemm_outlier", _lib.w8a8_gemm_outlier(_ptr(X), _ptr(W), _ptr(Sw), _ptr(Y), M, K, N, float(threshold),
+                                                       _ptr(Xq_out), _ptr(Sx_out), _ptr(acc_out),
+                                                       _ptr(n_outliers_out), _ptr(workspace), workspace_bytes,
+                                                       flags, _stream(stream)))
 
 
 def w8a8_gemm_noalloc_max_scratch_bytes() -> int:

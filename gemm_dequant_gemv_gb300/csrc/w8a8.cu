@@ -50,8 +50,11 @@ namespace {
 // CUDA", Smoothquant: Y = (X diag(s)^-1)(diag(s) W)); every activation is
 // divided by it (one correctly rounded fp32 division) before the row amax and
 // the codes.
+// out_flags (int [K] or null): LLM.int8()'s outlier columns, quantized as zero
+// here (their product runs in 16-bit floating point in the GEMM epilogue).
 __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restrict__ X, int K,
                                                          const float* __restrict__ smooth,
+                                                         const int* __restrict__ out_flags,
                                                          __half* __restrict__ xq16, float* __restrict__ sx_ws,
                                                          int8_t* __restrict__ xq_out, float* __restrict__ sx_out) {
   __shared__ float red[8];
@@ -71,6 +74,13 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
       const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[i] = __fdiv_rn(x[i], sv[i]);
+    }
+    if (out_flags) {
+      const int4 f0 = *reinterpret_cast<const int4*>(out_flags + k);
+      const int4 f1 = *reinterpret_cast<const int4*>(out_flags + k + 4);
+      const int fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = fv[i] ? 0.f : x[i];
     }
   };
   for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
@@ -120,6 +130,71 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
   pdl_launch_dependents();  // the GEMM may start once every row's codes are written
 }
 
+// --------------------------------------------------------- LLM.int8() scan --
+// ("Quantization CUDA", LLM.int8(): the activation columns holding a value
+// above the threshold, with the matching weight rows, are multiplied in 16-bit
+// floating point.)  flags[k] = 1 when some |X[m,k]| > threshold: one thread
+// covers 8 columns (one 16-byte load per row) over a chunk of 32 rows.
+__global__ void __launch_bounds__(256) w8a8_outlier_scan_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                float threshold, int* __restrict__ flags) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int k = (blockIdx.x * 256 + threadIdx.x) * 8;
+  if (k >= K) return;
+  const int m0 = blockIdx.y * 32, m1 = min(M, m0 + 32);
+  uint32_t hit = 0;  // bit i: column k + i
+  for (int m = m0; m < m1; ++m) {
+    const uint4 v = *reinterpret_cast<const uint4*>(X + size_t(m) * K + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (fabsf(bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu))) > threshold) hit |= 1u << i;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if ((hit >> i) & 1u) flags[k + i] = 1;
+}
+
+// The flagged columns in increasing order (idx) and their number (count, and
+// *count_out when given): one CTA, a block-wide exclusive scan of per-thread counts.
+__global__ void __launch_bounds__(1024) w8a8_outlier_compact_kernel(const int* __restrict__ flags, int K,
+                                                                    int* __restrict__ idx, int* __restrict__ count,
+                                                                    int* __restrict__ count_out) {
+  __shared__ int warp_sum[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int per = (K + 1023) / 1024;
+  const int k0 = min(K, int(threadIdx.x) * per), k1 = min(K, k0 + per);
+  int c = 0;
+  for (int k = k0; k < k1; ++k) c += flags[k] != 0;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = c;  // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int v = warp_sum[lane], wincl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += t;
+    }
+    warp_sum[lane] = wincl - v;  // exclusive prefix of the warp totals
+  }
+  __syncthreads();
+  int pos = warp_sum[wid] + incl - c;
+  for (int k = k0; k < k1; ++k)
+    if (flags[k]) idx[pos++] = k;
+  if (threadIdx.x == blockDim.x - 1) {
+    *count = pos;
+    if (count_out) *count_out = pos;
+  }
+}
+
 // --------------------------------------------------------------------- GEMM --
 // Roles: the tensor core computes D[n, m] = sum_k W[k, n] X[m, k] for a tile of
 // 128 columns n (MMA M, operand A = W^T in tensor memory) by 128 rows m (MMA N,
@@ -149,6 +224,8 @@ constexpr uint32_t kDCols = kBM;             // fp32 accumulator columns per buf
 constexpr uint32_t kACols = kBK / 2;         // 64 columns of fp16 pairs per W^T stage
 constexpr uint32_t kTmemCols = 2 * kDCols + kNS * kACols;  // 512
 constexpr int kOutStride = kBN * 2 + 16;     // padded bf16 output row in shared memory
+constexpr int kOutChunk = 32;                // outlier columns staged per round (LLM.int8())
+constexpr int kOutlierStage = 64 * 1024;     // their x [128 m][32] and w [32][128 n] fp32, in the X ring
 static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
 static_assert(kEpiCols == 64, "the epilogue loop reads 16-column groups of a 64-column half");
 
@@ -167,6 +244,9 @@ struct SmemW8A8 {
   }
 };
 static_assert(kBM * kOutStride <= kNS * kXBytes, "the output tile is staged in the X ring");
+static_assert(kBM * kOutStride <= kOutlierStage &&
+                  kOutlierStage + (kBM + kBN) * kOutChunk * 4 <= kNS * kXBytes,
+              "the outlier operands sit in the X ring after the output staging area");
 static_assert(kNS % kConvGroups == 0, "a stage slot is always refilled by the same converter group");
 
 struct W8A8Args {
@@ -174,6 +254,12 @@ struct W8A8Args {
   const float* Sx;       // workspace copy written by the quantization kernel
   void* Y;
   int32_t* acc_out;
+  // LLM.int8() (all null otherwise): the outlier columns and their number, and
+  // the bf16 activations and int8 weights their 16-bit product reads
+  const int* out_idx;
+  const int* out_count;
+  const uint16_t* Xb;
+  const int8_t* Wb;
   int M, K, N;
 };
 
@@ -185,6 +271,9 @@ __device__ __forceinline__ uint32_t quad_transpose(uint32_t w, uint32_t sel1, ui
   return prmt(y, __shfl_xor_sync(0xffffffffu, y, 1), sel2);
 }
 
+// OUTLIER: the LLM.int8() epilogue (a separate instance, so that the plain
+// GEMM carries none of its code or registers).
+template <bool OUTLIER>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_mma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                     const W8A8Args a) {
@@ -383,16 +472,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Y = bf16(Sx * acc * Sw) staged in shared memory (the X stages are free now:
     // the MMA warp saw the last one released before the epilogue's last chunk)
     asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // epilogue warps: sSx complete
-    uint16_t* ocol = reinterpret_cast<uint16_t*>(sX) + col;
     const bool col_ok = n0 + col < N;
+    // the int32 product (debug output), then y = (Sx * acc) * Sw in fp32, in place
 #pragma unroll
     for (int c = 0; c < kEpiCols; ++c) {
       const int r = cbase + c;
       const int32_t iv = static_cast<int32_t>(acc[c] - bias);
-      const float f = (sSx[r] * static_cast<float>(iv)) * sw;
-      ocol[size_t(r) * (kOutStride / 2)] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
       if (a.acc_out && col_ok && m0 + r < M) a.acc_out[size_t(m0 + r) * N + n0 + col] = iv;
+      acc[c] = __float_as_uint((sSx[r] * static_cast<float>(iv)) * sw);
     }
+    if (OUTLIER) {
+      // LLM.int8(): y += sum_j X[m, idx_j] * (Sw[n] * W[idx_j, n]) over the outlier
+      // columns, staged kOutChunk at a time in the (now free) X ring
+      const int cnt = *a.out_count;
+      float* xo = reinterpret_cast<float*>(sX + kOutlierStage);  // [kBM][kOutChunk]
+      float* wo = xo + kBM * kOutChunk;                           // [kOutChunk][kBN]
+      for (int j0 = 0; j0 < cnt; j0 += kOutChunk) {
+        const int nj = min(kOutChunk, cnt - j0);
+        asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // the previous round is consumed
+        for (int i = et; i < kBM * kOutChunk; i += kEpiThreads) {
+          const int m = i / kOutChunk, j = i % kOutChunk;
+          xo[i] = (j < nj && m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + a.out_idx[j0 + j]]) : 0.f;
+        }
+        for (int i = et; i < kOutChunk * kBN; i += kEpiThreads) {
+          const int j = i / kBN, n = i % kBN;
+          wo[i] = (j < nj && n0 + n < N) ? static_cast<float>(a.Wb[size_t(a.out_idx[j0 + j]) * N + n0 + n]) : 0.f;
+        }
+        asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
+        for (int j = 0; j < nj; ++j) {
+          const float sww = sw * wo[j * kBN + col];
+#pragma unroll
+          for (int c = 0; c < kEpiCols; ++c)
+            acc[c] = __float_as_uint(fmaf(xo[(cbase + c) * kOutChunk + j], sww, __uint_as_float(acc[c])));
+        }
+      }
+    }
+    uint16_t* ocol = reinterpret_cast<uint16_t*>(sX) + col;
+#pragma unroll
+    for (int c = 0; c < kEpiCols; ++c)
+      ocol[size_t(cbase + c) * (kOutStride / 2)] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(acc[c])));
     asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
     // coalesced stores: 16 chunks of 16 bytes per tile row
     uint16_t* Y = static_cast<uint16_t*>(a.Y);
@@ -436,18 +554,50 @@ size_t w8a8_workspace_bytes(int M, int K, int N) {
   return align_up(size_t(M) * K * 2, 256) + align_up(size_t(M) * 4, 256);
 }
 
+// LLM.int8() needs, after the plain workspace, the column flags and the list
+// of outlier columns (int [K] each) and their count.
+size_t w8a8_outlier_workspace_bytes(int M, int K, int N) {
+  const size_t base = w8a8_workspace_bytes(M, K, N);
+  if (base == 0) return 0;
+  return base + 2 * align_up(size_t(K) * 4, 256) + 256;
+}
+
 cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
                         int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
-                        cudaStream_t stream, const float* smooth) {
+                        cudaStream_t stream, const float* smooth, const float* outlier_threshold,
+                        int32_t* n_outliers_out) {
   const SmemW8A8 L;
   if (L.total > static_cast<size_t>(device_max_smem())) return cudaErrorNotSupported;
   __half* xq16 = static_cast<__half*>(workspace);
   float* sx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(size_t(M) * K * 2, 256));
+  const uint16_t* Xp = static_cast<const uint16_t*>(X);
+
+  // 0) LLM.int8(): flag the outlier columns and list them
+  int* oflags = nullptr;
+  int* oidx = nullptr;
+  int* ocount = nullptr;
+  if (outlier_threshold) {
+    uint8_t* o = static_cast<uint8_t*>(workspace) + w8a8_workspace_bytes(M, K, N);
+    oflags = reinterpret_cast<int*>(o);
+    oidx = reinterpret_cast<int*>(o + align_up(size_t(K) * 4, 256));
+    ocount = reinterpret_cast<int*>(o + 2 * align_up(size_t(K) * 4, 256));
+    cudaError_t e = cudaMemsetAsync(oflags, 0, size_t(K) * 4, stream);
+    if (e != cudaSuccess) return e;
+    float th = *outlier_threshold;
+    void* sargs[] = {&Xp, &M, &K, &th, &oflags};
+    e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_scan_kernel), dim3((K + 2047) / 2048, (M + 31) / 32),
+                  dim3(256), 0, flags, stream, sargs);
+    if (e != cudaSuccess) return e;
+    void* cargs[] = {&oflags, &K, &oidx, &ocount, &n_outliers_out};
+    e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_compact_kernel), dim3(1), dim3(1024), 0,
+                  flags | WQ_FLAG_PDL, stream, cargs);
+    if (e != cudaSuccess) return e;
+  }
 
   // 1) per-row quantization
   {
-    const uint16_t* Xp = static_cast<const uint16_t*>(X);
-    void* args[] = {&Xp, &K, &smooth, &xq16, &sx, &Xq_out, &Sx_out};
+    const int* of = oflags;
+    void* args[] = {&Xp, &K, &smooth, &of, &xq16, &sx, &Xq_out, &Sx_out};
     cudaError_t e = launch_ex(reinterpret_cast<const void*>(w8a8_quant_kernel), dim3(M), dim3(256), 0, flags, stream,
                               args);
     if (e != cudaSuccess) return e;
@@ -458,8 +608,10 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, N, K, N, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  W8A8Args args{Sw, sx, Y, acc_out, M, K, N};
-  const void* kern = reinterpret_cast<const void*>(w8a8_mma_kernel);
+  W8A8Args args{Sw, sx, Y, acc_out, oidx, ocount, outlier_threshold ? Xp : nullptr, outlier_threshold ? W : nullptr,
+                M, K, N};
+  const void* kern = outlier_threshold ? reinterpret_cast<const void*>(w8a8_mma_kernel<true>)
+                                       : reinterpret_cast<const void*>(w8a8_mma_kernel<false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
   void* kargs[] = {&xmap, &wmap, &args};

@@ -377,4 +377,23 @@ WQ_API wq_status w8a8_gemm_smooth(const void* X, const float* smooth, const int8
                                static_cast<cudaStream_t>(stream), smooth));
 }
 
+WQ_API size_t w8a8_gemm_outlier_workspace_bytes(int M, int K, int N) { return w8a8_outlier_workspace_bytes(M, K, N); }
+
+WQ_API wq_status w8a8_gemm_outlier(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
+                                   float threshold, int8_t* Xq_out, float* Sx_out, int32_t* acc_out,
+                                   int32_t* n_outliers_out, void* workspace, size_t workspace_bytes, unsigned flags,
+                                   void* stream) {
+  if (!X || !W || !Sw || !Y || !workspace) return (!workspace && X && W && Sw && Y) ? WQ_ERR_WORKSPACE : WQ_ERR_NULL;
+  if (M < 1 || K < 64 || N < 16 || M > kMaxDim || K > 65536 || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 64 != 0 || N % 16 != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Sw) || !aligned16(Y) || (Xq_out && !aligned16(Xq_out)) ||
+      (Sx_out && !aligned16(Sx_out)) || (acc_out && !aligned16(acc_out)) ||
+      (n_outliers_out && (reinterpret_cast<uintptr_t>(n_outliers_out) & 3u) != 0) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return WQ_ERR_ALIGN;
+  if (workspace_bytes < w8a8_outlier_workspace_bytes(M, K, N)) return WQ_ERR_WORKSPACE;
+  return from_cuda(launch_w8a8(X, W, Sw, Y, M, K, N, Xq_out, Sx_out, acc_out, workspace, flags,
+                               static_cast<cudaStream_t>(stream), nullptr, &threshold, n_outliers_out));
+}
+
 }  // extern "C"

@@ -16,9 +16,14 @@ cudaError_t launch_wq4_mma(const void* x, const int32_t* qweight, const void* sc
 size_t w8a8_workspace_bytes(int M, int K, int N);
 
 // smooth: Smoothquant's per-channel divisor of the activations (fp32 [K]), or null.
+// outlier_threshold: LLM.int8()'s threshold (host value), or null; then the
+// workspace holds w8a8_outlier_workspace_bytes and n_outliers_out (device,
+// optional) receives the number of outlier columns.
 cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
                         int8_t* Xq_out, float* Sx_out, int32_t* acc_out, void* workspace, unsigned flags,
-                        cudaStream_t stream, const float* smooth = nullptr);
+                        cudaStream_t stream, const float* smooth = nullptr,
+                        const float* outlier_threshold = nullptr, int32_t* n_outliers_out = nullptr);
+size_t w8a8_outlier_workspace_bytes(int M, int K, int N);
 
 // Act-order preparation (host-driven, synchronous on `stream`): 0 = ok,
 // 1 = g_idx is not a grouping with exactly `group` rows per group, 2 = CUDA error.

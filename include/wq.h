@@ -253,6 +253,34 @@ WQ_API wq_status w8a8_gemm_smooth(const void* X, const float* smooth, const int8
                                   void* workspace, size_t workspace_bytes, unsigned flags,
                                   void* stream);
 
+/*
+ * w8a8_gemm_outlier -- W8A8 with LLM.int8()'s mixed-precision decomposition
+ * ([QC] LLM.int8(): the activation columns holding a value above a threshold,
+ * with the matching weight rows, stay in 16-bit floating point; the rest goes
+ * through int8; the two results are added):
+ *   O        = { k : |X[m,k]| > threshold for some m }   (strictly greater)
+ *   Sx, Xq   = the row quantization of w8a8_gemm applied to X with the
+ *              columns in O set to zero (the regular part)
+ *   acc[m,n] = sum_k Xq[m,k] * W[k,n]                     (exact int32)
+ *   Y[m,n]   = bf16( (Sx[m]*acc[m,n])*Sw[n]
+ *                    + sum_{k in O} X[m,k] * (Sw[n]*W[k,n]) )  (fp32)
+ * The 16-bit part uses the activations as stored (bf16) and the weight rows
+ * dequantized from their int8 codes; it is added in fp32 before the single
+ * bf16 rounding of Y.  threshold: any float (the pages use 6.0; a negative
+ * value sends every column to the 16-bit part, +inf none).
+ *   n_outliers_out: device int32 or NULL, receives |O|.
+ *   workspace >= w8a8_gemm_outlier_workspace_bytes(M, K, N) bytes, 256-byte
+ *   aligned.  Other arguments, shapes and errors as in w8a8_gemm.
+ */
+WQ_API wq_status w8a8_gemm_outlier(const void* X, const int8_t* W, const float* Sw, void* Y,
+                                   int M, int K, int N, float threshold, int8_t* Xq_out,
+                                   float* Sx_out, int32_t* acc_out, int32_t* n_outliers_out,
+                                   void* workspace, size_t workspace_bytes, unsigned flags,
+                                   void* stream);
+
+/* Bytes of device workspace w8a8_gemm_outlier needs for this shape (0 on bad shape). */
+WQ_API size_t w8a8_gemm_outlier_workspace_bytes(int M, int K, int N);
+
 /* Bytes of device workspace w8a8_gemm needs for this shape (0 on bad shape). */
 WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
 

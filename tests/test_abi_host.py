@@ -154,6 +154,21 @@ def test_w8a8_smooth_validation(wq):
         assert f(*a) == want, edits
 
 
+def test_w8a8_outlier_validation(wq):
+    lib = wq.library()
+    f = lib.w8a8_gemm_outlier
+    need = lib.w8a8_gemm_outlier_workspace_bytes(128, 256, 256)
+    assert need > lib.w8a8_gemm_workspace_bytes(128, 256, 256)
+    ok = [A, A, A, A, 128, 256, 256, 6.0, None, None, None, None, A, need, 0, 0]
+    for edits, want in (({0: 0}, wq.WQ_ERR_NULL), ({5: 96}, wq.WQ_ERR_SHAPE), ({6: 40}, wq.WQ_ERR_SHAPE),
+                        ({11: A + 2}, wq.WQ_ERR_ALIGN), ({12: A + 16}, wq.WQ_ERR_ALIGN),
+                        ({13: need - 1}, wq.WQ_ERR_WORKSPACE)):
+        a = list(ok)
+        for i, v in edits.items():
+            a[i] = v
+        assert f(*a) == want, edits
+
+
 def test_w8a8_validation(wq):
     f = wq.library().w8a8_gemm
     need = wq.w8a8_gemm_workspace_bytes(64, 128, 64)

@@ -131,3 +131,43 @@ def test_w8a8_smooth_parity(G):
     # smoothing lowers the row scales that the outlier channels set
     _, Sx_plain = oracle.w8a8_quant_rows(X_bits)
     assert np.all(Sx_ref <= Sx_plain) and np.mean(Sx_ref) < 0.5 * np.mean(Sx_plain)
+
+
+@pytest.mark.parametrize("M,K,N,threshold", [(200, 512, 272, 6.0), (128, 8192, 256, 6.0), (64, 256, 128, -1.0),
+                                             (96, 320, 144, float("inf"))])
+def test_w8a8_outlier_parity(G, M, K, N, threshold):
+    """LLM.int8(): outlier columns flagged as the oracle flags them, Sx / Xq / the int8
+    part's int32 product bit-exact, Y (int8 part + 16-bit outlier part) under the bar."""
+    import torch
+    import gemm_dequant_gemv_gb300 as wq
+    import oracle
+    import synthetic as syn
+    from tolerance import U_BF16, within
+    r = np.random.default_rng(41 + K)
+    Xf = r.normal(0, 1, (M, K)).astype(np.float32)
+    cols = r.choice(K, size=min(40, K // 8), replace=False)   # more than one staging round of 32
+    for i, c in enumerate(cols):
+        Xf[r.integers(0, M), c] = (8.0 + i) * (1 if i % 2 else -1)
+    Xf[0, (cols[0] + 1) % K] = 6.0                               # equal to the threshold
+    X_bits = syn.f32_to_bf16_bits(Xf)
+    W = r.integers(-127, 128, (K, N), dtype=np.int8)
+    Sw = r.uniform(0.001, 0.01, N).astype(np.float32)
+    Xd, Wd, Swd = G.dev(X_bits), G.dev(W), G.dev(Sw)
+    buf, Y = G.guarded((M, N), torch.bfloat16)
+    Xq = torch.empty((M, K), dtype=torch.int8, device=G.DEV)
+    Sx = torch.empty((M,), dtype=torch.float32, device=G.DEV)
+    acc = torch.empty((M, N), dtype=torch.int32, device=G.DEV)
+    nout = torch.zeros((4,), dtype=torch.int32, device=G.DEV)
+    nb = wq.w8a8_gemm_outlier_workspace_bytes(M, K, N)
+    ws = torch.empty(nb, dtype=torch.uint8, device=G.DEV)
+    wq.w8a8_gemm_outlier(Xd, Wd, Swd, Y, M, K, N, threshold, Xq, Sx, acc, nout, ws, nb)
+    torch.cuda.synchronize()
+    G.check_canary(buf, M * N)
+    flags, Xq_ref, Sx_ref, acc_ref, y_ref, a, ovf = oracle.w8a8_outlier(X_bits, W, Sw, threshold)
+    assert int(nout[0]) == int(flags.sum())
+    assert np.array_equal(Sx.cpu().numpy().view(np.uint32), Sx_ref.view(np.uint32)), "Sx differs"
+    assert np.array_equal(Xq.cpu().numpy(), Xq_ref), "Xq differs"
+    assert not ovf
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), acc_ref), "int32 accumulator differs"
+    ok, worst = within(G.to_f64(Y), y_ref, a, U_BF16)
+    assert ok, f"max |err|/bound = {worst:.3g}"
