@@ -134,21 +134,28 @@ __global__ void __launch_bounds__(256) w8a8_quant_kernel(const uint16_t* __restr
 // ("Quantization CUDA", LLM.int8(): the activation columns holding a value
 // above the threshold, with the matching weight rows, are multiplied in 16-bit
 // floating point.)  flags[k] = 1 when some |X[m,k]| > threshold: one thread
-// covers 8 columns (one 16-byte load per row) over a chunk of 32 rows.
+// covers 8 columns (one 16-byte load per row) over a chunk of kScanRows rows,
+// all loads in flight at once.
+constexpr int kScanRows = 8;
 __global__ void __launch_bounds__(256) w8a8_outlier_scan_kernel(const uint16_t* __restrict__ X, int M, int K,
                                                                 float threshold, int* __restrict__ flags) {
   pdl_launch_dependents();
   pdl_wait();
   const int k = (blockIdx.x * 256 + threadIdx.x) * 8;
   if (k >= K) return;
-  const int m0 = blockIdx.y * 32, m1 = min(M, m0 + 32);
   uint32_t hit = 0;  // bit i: column k + i
-  for (int m = m0; m < m1; ++m) {
-    const uint4 v = *reinterpret_cast<const uint4*>(X + size_t(m) * K + k);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int m0 = blockIdx.y * kScanRows; m0 < M; m0 += gridDim.y * kScanRows) {  // grid-stride over row chunks
+    uint4 rows[kScanRows];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (fabsf(bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu))) > threshold) hit |= 1u << i;
+    for (int j = 0; j < kScanRows; ++j)
+      rows[j] = (m0 + j < M) ? *reinterpret_cast<const uint4*>(X + size_t(m0 + j) * K + k) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < kScanRows; ++j) {
+      const uint32_t w[4] = {rows[j].x, rows[j].y, rows[j].z, rows[j].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (fabsf(bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu))) > threshold) hit |= 1u << i;
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -245,7 +252,7 @@ struct SmemW8A8 {
 };
 static_assert(kBM * kOutStride <= kNS * kXBytes, "the output tile is staged in the X ring");
 static_assert(kBM * kOutStride <= kOutlierStage &&
-                  kOutlierStage + (kBM + kBN) * kOutChunk * 4 <= kNS * kXBytes,
+                  kOutlierStage + (kBM + kBN + 1) * kOutChunk * 4 <= kNS * kXBytes,
               "the outlier operands sit in the X ring after the output staging area");
 static_assert(kNS % kConvGroups == 0, "a stage slot is always refilled by the same converter group");
 
@@ -487,16 +494,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cnt = *a.out_count;
       float* xo = reinterpret_cast<float*>(sX + kOutlierStage);  // [kBM][kOutChunk]
       float* wo = xo + kBM * kOutChunk;                           // [kOutChunk][kBN]
+      int* sidx = reinterpret_cast<int*>(wo + kOutChunk * kBN);   // [kOutChunk] column indices
       for (int j0 = 0; j0 < cnt; j0 += kOutChunk) {
         const int nj = min(kOutChunk, cnt - j0);
         asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // the previous round is consumed
-        for (int i = et; i < kBM * kOutChunk; i += kEpiThreads) {
-          const int m = i / kOutChunk, j = i % kOutChunk;
-          xo[i] = (j < nj && m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + a.out_idx[j0 + j]]) : 0.f;
+        if (et < kOutChunk) sidx[et] = et < nj ? a.out_idx[j0 + et] : 0;
+        asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
+        // every gather of the round in flight at once
+#pragma unroll
+        for (int t = 0; t < kBM * kOutChunk / kEpiThreads; ++t) {
+          const int i = et + t * kEpiThreads, m = i / kOutChunk, j = i % kOutChunk;
+          xo[i] = (j < nj && m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + sidx[j]]) : 0.f;
         }
-        for (int i = et; i < kOutChunk * kBN; i += kEpiThreads) {
-          const int j = i / kBN, n = i % kBN;
-          wo[i] = (j < nj && n0 + n < N) ? static_cast<float>(a.Wb[size_t(a.out_idx[j0 + j]) * N + n0 + n]) : 0.f;
+#pragma unroll
+        for (int t = 0; t < kOutChunk * kBN / kEpiThreads; ++t) {
+          const int i = et + t * kEpiThreads, j = i / kBN, n = i % kBN;
+          wo[i] = (j < nj && n0 + n < N) ? static_cast<float>(a.Wb[size_t(sidx[j]) * N + n0 + n]) : 0.f;
         }
         asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
         for (int j = 0; j < nj; ++j) {
@@ -585,7 +598,8 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
     if (e != cudaSuccess) return e;
     float th = *outlier_threshold;
     void* sargs[] = {&Xp, &M, &K, &th, &oflags};
-    e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_scan_kernel), dim3((K + 2047) / 2048, (M + 31) / 32),
+    e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_scan_kernel),
+                  dim3((K + 2047) / 2048, std::min((M + kScanRows - 1) / kScanRows, 65535)),
                   dim3(256), 0, flags, stream, sargs);
     if (e != cudaSuccess) return e;
     void* cargs[] = {&oflags, &K, &oidx, &ocount, &n_outliers_out};
