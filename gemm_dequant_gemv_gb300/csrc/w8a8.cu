@@ -17,8 +17,11 @@
 // the end, in wrapping unsigned arithmetic).  The int32 result is never
 // stored unless a debug output is requested.
 //
-// Kernels: (1) w8a8_quant_kernel, one CTA per row: Sx, the int8 codes (if
-// requested) and fp16 copies of the codes in the workspace; (2)
+// Kernels: (0) LLM.int8() only: w8a8_outlier_scan_kernel flags the columns of
+// X holding a value above the threshold, w8a8_outlier_compact_kernel lists
+// them; (1) w8a8_quant_kernel, one CTA per row: Sx, the int8 codes (if
+// requested) and fp16 copies of the codes in the workspace, after the optional
+// Smoothquant division and with LLM.int8()'s outlier columns zeroed; (2)
 // w8a8_mma_kernel, one 128 x 128 output tile per CTA, 128-value k stages:
 //   warp 16 : TMA of the int8 W tile (lane 0, before the dependency wait) and
 //             of the fp16 X code tile (lane 1), both 128-byte swizzled;
@@ -28,7 +31,9 @@
 //             memory, B = X from shared memory, into one of two tensor-memory
 //             accumulators (one per 256-value chunk of k);
 //   warps 8-15 : drain each chunk into int32 and, at the end, write
-//             Y = bf16(Sx * acc * Sw) through shared memory with coalesced stores.
+//             Y = bf16(Sx * acc * Sw) through shared memory with coalesced stores
+//             (the LLM.int8() instance adds the outlier columns' 16-bit product
+//             in fp32 first).
 #include <algorithm>
 
 #include "../../include/wq.h"
