@@ -505,11 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // the previous round is consumed
         if (et < kOutChunk) sidx[et] = et < nj ? a.out_idx[j0 + et] : 0;
         asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
-        // every gather of the round in flight at once
+        // the kBM x nj real activations spread over every thread, all loads in flight at once
+        // (slots j >= nj are never read)
 #pragma unroll
         for (int t = 0; t < kBM * kOutChunk / kEpiThreads; ++t) {
-          const int i = et + t * kEpiThreads, m = i / kOutChunk, j = i % kOutChunk;
-          xo[i] = (j < nj && m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + sidx[j]]) : 0.f;
+          const int i = et + t * kEpiThreads;
+          if (i < kBM * nj) {
+            const int m = i / nj, j = i % nj;
+            xo[m * kOutChunk + j] = (m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + sidx[j]]) : 0.f;
+          }
         }
 #pragma unroll
         for (int t = 0; t < kOutChunk * kBN / kEpiThreads; ++t) {
