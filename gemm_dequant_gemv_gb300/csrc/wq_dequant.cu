@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(kThreads) dq4_kernel(const int32_t* __restrict
 }
 
 cudaError_t launch_simple(const void* kern, size_t items, unsigned flags, cudaStream_t stream, void** args) {
-  const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  const int n_sm = device_sm_count();
+  const int sms = n_sm > 0 ? n_sm : 1;
   const size_t want = (items + kThreads - 1) / kThreads;
   const unsigned grid = static_cast<unsigned>(want < size_t(8) * sms ? (want > 0 ? want : 1) : size_t(8) * sms);
   cudaLaunchConfig_t cfg = {};

@@ -152,6 +152,14 @@ def round_f16(y: np.ndarray) -> np.ndarray:
     return out.reshape(np.shape(y))
 
 
+def round_f32(y: np.ndarray) -> np.ndarray:
+    """Round an array of doubles to fp32 (RNE, the C conversion)."""
+    lib = _load()
+    flat = np.asarray(y, dtype=np.float64).ravel()
+    out = np.fromiter((lib.wqo_double_to_f32(float(v)) for v in flat), dtype=np.float32, count=flat.size)
+    return out.reshape(np.shape(y))
+
+
 def round_bf16(y: np.ndarray) -> np.ndarray:
     """Round an array of doubles to bf16 bit patterns (uint16), RNE."""
     lib = _load()
