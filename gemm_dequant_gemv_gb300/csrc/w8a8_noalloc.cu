@@ -15,8 +15,8 @@ namespace wq {
 namespace {
 
 // Largest scratch the built-in array offers: 8 MiB.  w8a8_gemm needs
-// align256(2*M*K) + align256(4*M) bytes, so M*K up to about 4.19 million
-// (for example M = 512 at K = 8192, or M = 1024 at K = 4096).
+// align256(2*M*K) + align256(4*M) bytes, so for example M <= 511 at K = 8192
+// or M <= 1023 at K = 4096 (M = 512 at K = 8192 needs 8 MiB + 2048 bytes).
 constexpr size_t kScratchBytes = size_t(8) << 20;
 
 // The scratch itself, one copy per device (module-scope device memory).

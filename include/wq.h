@@ -297,8 +297,9 @@ WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
  *   library, one copy per device, of w8a8_gemm_noalloc_max_scratch_bytes()
  *   bytes (8 MiB).
  * Arguments, layouts, results and checks: as w8a8_gemm, without `workspace`.
- * Size limit: the shape's w8a8_gemm_workspace_bytes(M, K, N) must not exceed
- *   the built-in size (about M*K <= 4.19 million, e.g. M = 512 at K = 8192);
+ * Size limit: the shape's w8a8_gemm_workspace_bytes(M, K, N) =
+ *   align256(2*M*K) + align256(4*M) must not exceed the built-in size (for
+ *   example M <= 511 at K = 8192, M <= 1023 at K = 4096);
  *   a larger shape returns WQ_ERR_WORKSPACE before anything runs -- use
  *   w8a8_gemm with a workspace of your own for it.
  * First call on each device: looks up the device address of the built-in
@@ -311,7 +312,9 @@ WQ_API size_t w8a8_gemm_workspace_bytes(int M, int K, int N);
  * Concurrency: all calls on one device share the one scratch array.  Calls
  *   whose executions can overlap -- on different streams without an ordering
  *   between them, from any thread -- race on it and may return wrong
- *   results.  Calls issued on one stream (or otherwise ordered) are safe.
+ *   results.  Calls issued on one stream (or otherwise ordered) are safe,
+ *   also back to back with WQ_FLAG_PDL: the call's first kernel waits for the
+ *   preceding grid on the stream to complete before it writes the scratch.
  */
 WQ_API wq_status w8a8_gemm_noalloc(const void* X, const int8_t* W, const float* Sw, void* Y,
                                    int M, int K, int N, int8_t* Xq_out, float* Sx_out,

@@ -77,10 +77,24 @@ def test_w8a8_adversarial_full_magnitude(G):
     _check(G, syn.f32_to_bf16_bits(Xf), W, Sw)
 
 
+def full_workload_rows(M=2048, tile=128, n=256, seed=0):
+    """Both sides of every 128-row tile edge, the first and last rows, and seeded
+    random rows up to n in all."""
+    edges = {0, M - 1}
+    for e in range(tile, M, tile):
+        edges.update((e - 1, e))
+    r = np.random.default_rng(seed)
+    rest = r.permutation(np.setdiff1d(np.arange(M), sorted(edges)))[: n - len(edges)]
+    return np.sort(np.concatenate([np.array(sorted(edges)), rest])).astype(np.int64)
+
+
 def test_w8a8_full_workload_sampled_rows(G):
+    """The benchmarked 2048 x 8192 x 8192 shape: every row's Sx and Xq, and the
+    int32 product and Y of 256 rows (every tile edge and seeded random rows)."""
     import synthetic as syn
     d = syn.make_w8a8(seed=5)
-    rows = [0, 1, 127, 128, 129, 1000, 1023, 1024, 2046, 2047]
+    rows = full_workload_rows()
+    assert len(rows) == 256 and {127, 128, 1919, 1920, 2047} <= set(rows.tolist())
     _check(G, d["X"], d["W"], d["Sw"], rows)
 
 
