@@ -42,6 +42,8 @@ SIGNATURES = {
     "w8a8_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
     "w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P]),
     "w8a8_gemm_noalloc_max_scratch_bytes": (_SZ, []),
+    "wq4_repack_tiled": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "wq4_gemm_tiled": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _U, _P]),
 }
 
 
@@ -133,6 +135,18 @@ def wq4_gemm_sorted(x, qweight_sorted, scales, qzeros, perm, y, M, K, N, group_s
     _check("wq4_gemm_sorted", _lib.wq4_gemm_sorted(_ptr(x), _ptr(qweight_sorted), _ptr(scales), _ptr(qzeros),
                                                    _ptr(perm), _ptr(y), M, K, N, group_size, act_dtype, flags,
                                                    _stream(stream)))
+
+
+def wq4_repack_tiled(qweight, g_idx, K, N, group_size, qweight_tiled, perm=None, stream=None):
+    _check("wq4_repack_tiled", _lib.wq4_repack_tiled(_ptr(qweight), _ptr(g_idx), K, N, group_size,
+                                                     _ptr(qweight_tiled), _ptr(perm), _stream(stream)))
+
+
+def wq4_gemm_tiled(x, qweight_tiled, scales, qzeros, perm, y, M, K, N, group_size, act_dtype, flags=0,
+                   stream=None):
+    _check("wq4_gemm_tiled", _lib.wq4_gemm_tiled(_ptr(x), _ptr(qweight_tiled), _ptr(scales), _ptr(qzeros),
+                                                 _ptr(perm), _ptr(y), M, K, N, group_size, act_dtype, flags,
+                                                 _stream(stream)))
 
 
 def wq8_dequant(w, scales, w_out, K, N, group_size, flags=0, stream=None):

@@ -253,6 +253,11 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
                                     static_cast<cudaStream_t>(stream)));
   }
 
+  if (!g_idx && K % wq4t_unit_k() == 0 && group_size % wq4t_unit_k() == 0) {
+    const cudaError_t e = launch_wq4t(x, qweight, nullptr, scales, qzeros, nullptr, y, M, K, N, group_size, act_bf16,
+                                      flags, static_cast<cudaStream_t>(stream));
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
   if (!g_idx && M >= 2 && group_size % wq4m_unit_k() == 0)
     return wq4m_launch(x, qweight, scales, qzeros, nullptr, y, M, K, N, group_size, act_bf16, flags,
                        static_cast<cudaStream_t>(stream));
@@ -294,6 +299,11 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
   if (!aligned16(x) || !aligned16(qweight_sorted) || !aligned16(scales) || !aligned16(perm) || !aligned16(y) ||
       (qzeros && !aligned16(qzeros)))
     return WQ_ERR_ALIGN;
+  if (K % wq4t_unit_k() == 0 && group_size % wq4t_unit_k() == 0) {
+    const cudaError_t e = launch_wq4t(x, qweight_sorted, nullptr, scales, qzeros, perm, y, M, K, N, group_size,
+                                      act_dtype == WQ_BF16, flags, static_cast<cudaStream_t>(stream));
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
   if (M >= 2 && group_size % wq4m_unit_k() == 0)
     return wq4m_launch(x, qweight_sorted, scales, qzeros, perm, y, M, K, N, group_size, act_dtype == WQ_BF16, flags,
                        static_cast<cudaStream_t>(stream));
@@ -309,6 +319,34 @@ WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, c
       !encode_x_map(&pmap, CU_TENSOR_MAP_DATA_TYPE_INT32, perm, K, 1, 4, wq4_stage_k(), 1))
     return WQ_ERR_CUDA;
   return from_cuda(launch_wq4_gemv(p, wmap, pmap, nullptr, a, act_dtype == WQ_BF16, qzeros != nullptr, true));
+}
+
+WQ_API wq_status wq4_repack_tiled(const int32_t* qweight, const int32_t* g_idx, int K, int N, int group_size,
+                                  int32_t* qweight_tiled, int32_t* perm, void* stream) {
+  if (!qweight || !qweight_tiled || (g_idx && !perm)) return WQ_ERR_NULL;
+  if (K < 64 || N < 32 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 64 != 0 || N % 32 != 0 || group_size < 64 || group_size % 64 != 0 || K % group_size != 0)
+    return WQ_ERR_SHAPE;
+  if (!aligned16(qweight) || !aligned16(qweight_tiled) || (g_idx && (!aligned16(g_idx) || !aligned16(perm))))
+    return WQ_ERR_ALIGN;
+  const int r = repack_tiled(qweight, g_idx, K, N, group_size, qweight_tiled, g_idx ? perm : nullptr,
+                             static_cast<cudaStream_t>(stream));
+  return r == 0 ? WQ_OK : (r == 1 ? WQ_ERR_SHAPE : WQ_ERR_CUDA);
+}
+
+WQ_API wq_status wq4_gemm_tiled(const void* x, const int32_t* qweight_tiled, const void* scales,
+                                const int32_t* qzeros, const int32_t* perm, void* y, int M, int K, int N,
+                                int group_size, int act_dtype, unsigned flags, void* stream) {
+  if (!x || !qweight_tiled || !scales || !y) return WQ_ERR_NULL;
+  if (M < 1 || M > 8 || K < 64 || N < 32 || K > kMaxDim || N > kMaxDim) return WQ_ERR_SHAPE;
+  if (K % 64 != 0 || N % 32 != 0 || group_size < 64 || group_size % 64 != 0 || K % group_size != 0)
+    return WQ_ERR_SHAPE;
+  if (act_dtype != WQ_F16 && act_dtype != WQ_BF16) return WQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qweight_tiled) || !aligned16(scales) || !aligned16(y) ||
+      (qzeros && !aligned16(qzeros)) || (perm && !aligned16(perm)))
+    return WQ_ERR_ALIGN;
+  return from_cuda(launch_wq4t(x, nullptr, reinterpret_cast<const uint8_t*>(qweight_tiled), scales, qzeros, perm, y,
+                               M, K, N, group_size, act_dtype == WQ_BF16, flags, static_cast<cudaStream_t>(stream)));
 }
 
 WQ_API wq_status wq8_dequant(const int8_t* w, const float* scales, float* w_out, int K, int N, int group_size,

@@ -102,6 +102,14 @@ __device__ __forceinline__ void drain_stages(uint64_t* full, int issued) {
   }
 }
 
+// As drain_stages, for a ring whose depth is a run-time value.
+__device__ __forceinline__ void drain_stages_rt(uint64_t* full, int NS, int issued) {
+  for (int s = 0; s < NS && s < issued; ++s) {
+    const int last = ((issued - 1 - s) / NS) * NS + s;
+    mbar_wait(&full[s], (last / NS) & 1);
+  }
+}
+
 // Cross-warp / cross-CTA reduction without CTA-wide barriers.
 //
 // The tile's BN columns are split into S column chunks of `chunk` columns

@@ -54,6 +54,27 @@ size_t wq4m_gemv_smem_bytes(int MT, int ng_max, int S, bool perm, int K);
 cudaError_t launch_wq4m_gemv(const LaunchPlan& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                              const GemvArgs& a, int act_bf16, bool has_z, bool perm);
 
+// 4-bit GEMV on the warp-level tensor-core MMA with variable-width column
+// tiles (wq_gemv4t.cu); the tile shape and K-split are planned per call.
+struct Plan4T {
+  int nslab, S, T, NS, MT;
+};
+int wq4t_unit_k();
+// qweight: GPTQ layout [K/8, N] (wtiled == nullptr), or wtiled: the layout of
+// wq4_repack_tiled; perm != nullptr: rows sorted by act-order group.
+// Returns cudaErrorNotSupported for shapes this kernel does not take (M > 8,
+// K % 64, a group that is not 64 times a power of two, shared memory).
+cudaError_t launch_wq4t(const void* x, const int32_t* qweight, const uint8_t* wtiled, const void* scales,
+                        const int32_t* qzeros, const int32_t* perm, void* y, int M, int K, int N, int group,
+                        int act_bf16, unsigned flags, cudaStream_t stream);
+
+// Device queries and tensor-map encoding (wq_api.cu).
+int device_sm_count();
+int device_max_smem();
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle);
+
 // Standalone dequantization to a dense [K, N] matrix (wq_dequant.cu).
 cudaError_t launch_wq8_dequant(const int8_t* w, const float* scales, float* out, int K, int N, int group,
                                unsigned flags, cudaStream_t stream);

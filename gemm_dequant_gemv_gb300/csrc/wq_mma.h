@@ -27,6 +27,12 @@ size_t w8a8_outlier_workspace_bytes(int M, int K, int N);
 
 // Act-order preparation (host-driven, synchronous on `stream`): 0 = ok,
 // 1 = g_idx is not a grouping with exactly `group` rows per group, 2 = CUDA error.
+// The tensor-core GEMV's tiled layout (host-driven, synchronous on `stream`):
+// rows sorted by group first when g_idx != null (perm written then); same
+// return codes as actorder_prepare.
+int repack_tiled(const int32_t* qweight, const int32_t* g_idx, int K, int N, int group, int32_t* qweight_tiled,
+                 int32_t* perm, cudaStream_t stream);
+
 int actorder_prepare(const int32_t* qweight, const int32_t* g_idx, int K, int N, int group, int32_t* qweight_sorted,
                      int32_t* perm, cudaStream_t stream);
 

@@ -134,7 +134,9 @@ WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
  *   g_idx  int32 [K] with values in [0, K/group), or NULL
  *   y      act_dtype [M, N]
  *   act_dtype: WQ_F16 or WQ_BF16.  M >= 1; K % group == 0, group % 32 == 0;
- *   N % 8 == 0.  M <= 8 runs on CUDA cores (any g_idx).  M > 8 runs on the
+ *   N % 8 == 0.  M <= 8 without g_idx runs on the warp-level tensor-core MMA
+ *   when K % 64 == 0 and group % 64 == 0, else on CUDA cores; with g_idx it
+ *   runs on CUDA cores (a scale gathered per code).  M > 8 runs on the
  *   tcgen05 tensor cores in chunks of up to 64 rows (padded to 16, 32 or 64)
  *   and needs group % 64 == 0 and g_idx == NULL; otherwise it returns
  *   WQ_ERR_UNSUPPORTED.
@@ -177,6 +179,43 @@ WQ_API wq_status wq4_actorder_prepare(const int32_t* qweight, const int32_t* g_i
 WQ_API wq_status wq4_gemm_sorted(const void* x, const int32_t* qweight_sorted, const void* scales,
                                  const int32_t* qzeros, const int32_t* perm, void* y, int M, int K,
                                  int N, int group_size, int act_dtype, unsigned flags, void* stream);
+
+/*
+ * wq4_repack_tiled -- one-time repack of 4-bit weights into the tile order of
+ * the tensor-core GEMV (the offline weight reshuffle that "Quantization CUDA",
+ * Marlin 格式 describes: a layout chosen so that the kernel's loads and the
+ * MMA fragments line up; this layout is this library's own).
+ *   Word (r, n) of the [K/8, N] matrix moves to
+ *     ((r/8) * (N/32) + n/32) * 256 + ((r%8) % 2) * 128 + (4 ((n%32)/4) + (r%8)/2) * 4 + n%4
+ *   so that each 64-value unit of k of each 32-column slab is one contiguous
+ *   1 KB block and the blocks of one unit follow each other over the slabs.
+ *   The codes inside each word are unchanged (nibble j = row 8r + j).
+ *   qweight       int32 [K/8, N]  input (device), the wq4_gemm layout
+ *   g_idx         int32 [K] or NULL (device): when given, the rows are first
+ *                 sorted by group as wq4_actorder_prepare does (every group
+ *                 must hold exactly group_size rows, else WQ_ERR_SHAPE), and
+ *                 perm (int32 [K], device, output) receives the sort;
+ *                 when NULL, perm is ignored and may be NULL
+ *   qweight_tiled int32, (K/8) * N words, output (device)
+ *   K % 64 == 0, N % 32 == 0, group_size % 64 == 0, K % group_size == 0.
+ * Synchronous on `stream`; not for a hot path.
+ */
+WQ_API wq_status wq4_repack_tiled(const int32_t* qweight, const int32_t* g_idx, int K, int N,
+                                  int group_size, int32_t* qweight_tiled, int32_t* perm, void* stream);
+
+/*
+ * wq4_gemm_tiled -- wq4_gemm (perm == NULL) or wq4_gemm_sorted (perm != NULL,
+ * the perm written by wq4_repack_tiled) on weights repacked by
+ * wq4_repack_tiled; same result, same scales and qzeros layouts.  Each
+ * pipeline stage of a CTA's slab is one contiguous bulk copy.
+ *   1 <= M <= 8; K % 64 == 0, N % 32 == 0, group_size = 64 * 2^j (64, 128,
+ *   256, ...), K % group_size == 0; with perm, the CTA's K-slice of x is
+ *   gathered into shared memory beside the pipeline; shapes whose shared
+ *   memory does not fit return WQ_ERR_UNSUPPORTED.
+ */
+WQ_API wq_status wq4_gemm_tiled(const void* x, const int32_t* qweight_tiled, const void* scales,
+                                const int32_t* qzeros, const int32_t* perm, void* y, int M, int K,
+                                int N, int group_size, int act_dtype, unsigned flags, void* stream);
 
 /*
  * wq8_dequant / wq3_dequant / wq4_dequant -- standalone dequantization: the

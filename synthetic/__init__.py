@@ -116,6 +116,30 @@ def pack4(codes: np.ndarray) -> np.ndarray:
     return w.view(np.int32)
 
 
+def tile4_index(K: int, N: int) -> np.ndarray:
+    """Destination of every word of a [K/8, N] 4-bit matrix in the library's
+    tiled layout (wq4_repack_tiled): word (r, n) goes to
+    ((r//8) * (N//32) + n//32) * 256 + ((r%8) % 2) * 128 + (4 * ((n%32)//4) + (r%8)//2) * 4 + n%4."""
+    assert K % 64 == 0 and N % 32 == 0
+    r = np.arange(K // 8, dtype=np.int64)[:, None]
+    n = np.arange(N, dtype=np.int64)[None, :]
+    rr = r % 8
+    return (((r // 8) * (N // 32) + n // 32) * 256 + (rr % 2) * 128 + (4 * ((n % 32) // 4) + rr // 2) * 4 + n % 4)
+
+
+def tile4(qweight: np.ndarray) -> np.ndarray:
+    """The tiled layout of a packed [K/8, N] 4-bit matrix (a flat int32 array)."""
+    R, N = qweight.shape
+    out = np.empty(R * N, dtype=qweight.dtype)
+    out[tile4_index(8 * R, N).ravel()] = qweight.ravel()
+    return out
+
+
+def untile4(tiled: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Inverse of tile4: the [K/8, N] matrix back from the tiled words."""
+    return np.asarray(tiled).ravel()[tile4_index(K, N)]
+
+
 def pack3(codes: np.ndarray) -> np.ndarray:
     """uint8 codes [K, N] in 0..7 -> int32 [3K/32, N] (96-bit little-endian blocks)."""
     codes = np.asarray(codes)
