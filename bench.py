@@ -44,10 +44,15 @@ LAYERS = 16
 WORKLOAD = ("decode step through 16 layers, each: W8 g128 GEMV 4096x4096 (fp32) + W3 per-column GEMV "
             "4096x4096 (fp16) + W4 act-order g128 GEMV 4096x11008 (fp16), M=1")
 FALLBACK_HBM_GBS = 6800.0
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the roofline kernel
-# (k4_gemv_kernel, sorted rows, 4096 x 11008, M = 1), from one ncu --set full capture
-# of that kernel under this script's own command; set to None when that kernel changes.
-K4_SORTED_TRAFFIC_BYTES = 23479808
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of each kernel of the
+# step, from one ncu capture of this script's own command; None until the kernel
+# as it is now has been captured (a capture of an older version does not count).
+TRAFFIC_BYTES = {"w8": None, "w3": None, "w4": None}
+KERNEL_NAMES = {
+    "w8": "k8_gemv_kernel<1> (W8 g128 GEMV 4096x4096, fp32 x)",
+    "w3": "k3_gemv_kernel<1> (W3 per-column GEMV 4096x4096, fp16 x)",
+    "w4": "k4t_gemv_kernel<f16, zeros, perm> (W4 act-order GEMV 4096x11008 on group-sorted rows, mma.sync)",
+}
 
 
 def alg_bytes_w8(M=1, K=4096, N=4096, g=128):
@@ -303,13 +308,25 @@ def run_ours(args, rank, world, dev):
             torch.cuda.synchronize(dev)
             w4_us += [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(LAYERS)]
 
-    # the roofline kernel's average launch duration where it runs chained: its 16
-    # launches (one per layer) back to back with PDL, one event pair around them
-    g_w4 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_w4, stream=stream, capture_error_mode="relaxed"):
-        for L in layers:
-            L.run_w4(wq, PDL, s)
-    w4_chain_us = _time_graph(g_w4, stream, 50, dev) * 1e3 / LAYERS
+    # every kernel of the step on its own: its 16 launches (one per layer) back to
+    # back, chained with PDL as in the step ("chained"), and the same 16 launches
+    # without PDL, so that each starts only after the previous one has finished
+    # ("serialized": the single-call latency on the device)
+    def kernel_times(run):
+        out = {}
+        for name, flags in (("chained", PDL), ("serialized", 0)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for L in layers:
+                    run(L, flags)
+            out[name] = _time_graph(g, stream, 50, dev) * 1e3 / LAYERS
+        return out
+    per_kernel = {
+        "w8": kernel_times(lambda L, f: L.run_w8(wq, f, s)),
+        "w3": kernel_times(lambda L, f: L.run_w3(wq, f, s)),
+        "w4": kernel_times(lambda L, f: L.run_w4(wq, f, s)),
+    }
+    w4_chain_us = per_kernel["w4"]["chained"]
 
     # the online act-order kernel (g_idx gathered per k, no prepared copy), chained over the layers
     g_on = torch.cuda.CUDAGraph()
@@ -353,7 +370,8 @@ def run_ours(args, rank, world, dev):
     te = time.perf_counter() - te
     te = max_over_ranks(te, world, dev)
 
-    return dict(ms=ms, w4_us=w4_us, w4_chain_us=w4_chain_us, w4_online_us=w4_online_us, clocks=clk.summary(),
+    return dict(ms=ms, w4_us=w4_us, w4_chain_us=w4_chain_us, w4_online_us=w4_online_us, per_kernel=per_kernel,
+                clocks=clk.summary(),
                 step_bytes=step_bytes,
                 e2e_s_per_step=te / e2e_steps, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps)
 
@@ -376,23 +394,52 @@ def sample_bytes(n8, n3, n4):
     return (alg_bytes_w8() * n8 / 4096 + alg_bytes_w3() * n3 / 4096 + alg_bytes_w4g() * n4 / 11008)
 
 
+def host_cores():
+    """Host core count and the cores this process may run on."""
+    try:
+        allowed = sorted(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        allowed = list(range(os.cpu_count() or 1))
+    return os.cpu_count() or len(allowed), allowed
+
+
+def pin_to_one_core():
+    """Pin the calling thread to one allowed core (the oracle is single-threaded);
+    returns that core, or None where the platform has no affinity call."""
+    _, allowed = host_cores()
+    try:
+        os.sched_setaffinity(0, {allowed[-1]})
+        return allowed[-1]
+    except (AttributeError, OSError):
+        return None
+
+
 def cpu_baseline(budget_s=10.0):
-    """The oracle as it stands, single-threaded, on whole steps of one layer."""
+    """The oracle as it stands, single-threaded and pinned to one core, on whole
+    steps of one layer."""
     import oracle
     oracle.build()
     d8, d3, d4 = make_layer_inputs(0)
-    t = time.perf_counter()
-    n = 0
-    while True:
-        oracle_step(d8, d3, d4)
-        n += 1
-        if time.perf_counter() - t >= budget_s:
-            break
-    dt = time.perf_counter() - t
+    total, allowed = host_cores()
+    saved = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    core = pin_to_one_core()
+    try:
+        t = time.perf_counter()
+        n = 0
+        while True:
+            oracle_step(d8, d3, d4)
+            n += 1
+            if time.perf_counter() - t >= budget_s:
+                break
+        dt = time.perf_counter() - t
+    finally:
+        if saved is not None:
+            os.sched_setaffinity(0, saved)
     b = n * sample_bytes(4096, 4096, 11008)
     return {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host_cores": total, "affinity_cores": len(allowed), "pinned_core": core,
             "sample": f"{n} full single-layer steps (W8 + W3 + W4 act-order GEMVs, every output column), "
-                      f"{dt:.1f} s single-threaded C oracle"}
+                      f"{dt:.1f} s single-threaded C oracle pinned to one of the host's {total} cores"}
 
 
 def run_reference(args):
@@ -403,6 +450,8 @@ def run_reference(args):
     import oracle
     oracle.build()
     d8, d3, d4 = make_layer_inputs(0)
+    total, allowed = host_cores()
+    core = pin_to_one_core()
     r = np.random.default_rng(0)
     probe = r.choice(4096, 64, replace=False)
     t = time.perf_counter()
@@ -427,7 +476,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "layers": 1, "M": 1, "sample_columns": ncols},
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_cores": total, "affinity_cores": len(allowed), "pinned_core": core},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -479,11 +529,11 @@ def run_wq4_sweep(args, dev):
                 c = r % copies
                 wq.wq4_gemm(x, qws[c], scs[c], None, None, y, M, K, N, g, wq.WQ_BF16, flags=wq.WQ_FLAG_PDL,
                             stream=stream)
-        ms = _time_graph(graph, stream, max(3, args.steps // 100), dev) / per
+        ms = _time_graph(graph, stream, args.extra_reps, dev) / per
         nbytes = (K // 8) * N * 4 + (K // g) * N * 2 + M * K * 2 + M * N * 2
         gbs = nbytes / (ms * 1e-3) / 1e9
         lines.append({"workload": f"W4A16 sym g128 K={K} N={N} M={M}", "M": M,
-                      "path": "cuda-core FFMA2" if M == 1 else ("mma.sync m16n8k16" if M <= 8 else "tcgen05"),
+                      "path": "mma.sync m16n8k16 (warp-level tensor cores)" if M <= 8 else "tcgen05 (tensor memory)",
                       "us_per_call": ms * 1e3,
                       "achieved_GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": peak_kind,
                       "tflops": 2 * M * K * N / (ms * 1e-3) / 1e12})
@@ -512,7 +562,7 @@ def run_w8a8(args, dev):
         for _ in range(per):
             wq.w8a8_gemm(X, W, Sw, Y, M, K, N, workspace=ws, workspace_bytes=nbytes, flags=wq.WQ_FLAG_PDL,
                          stream=stream)
-    ms = _time_graph(graph, stream, max(3, args.steps // 400), dev) / per
+    ms = _time_graph(graph, stream, args.extra_reps, dev) / per
     pk, pk_kind = measured_bf16_peak()
     tf = 2 * M * K * N / (ms * 1e-3) / 1e12
     lines = [{"workload": f"W8A8 dynamic quant GEMM M={M} K={K} N={N}", "us_per_call": ms * 1e3, "tops": tf,
@@ -550,7 +600,7 @@ def run_w8a8(args, dev):
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
             for _ in range(per):
                 fn(wq.WQ_FLAG_PDL)
-        msv = _time_graph(g, stream, max(3, args.steps // 400), dev) / per
+        msv = _time_graph(g, stream, args.extra_reps, dev) / per
         line = {"workload": f"W8A8 M={M} K={K} N={N}, {name}", "us_per_call": msv * 1e3,
                 "overhead_vs_plain": msv / ms - 1, "tops": 2 * M * K * N / (msv * 1e-3) / 1e12}
         if fn is outlier:
@@ -690,6 +740,10 @@ def main():
                     help="seconds of oracle work the reference arm aims for")
     ap.add_argument("--workload", default="gemv_step", choices=["gemv_step", "wq4_sweep", "w8a8", "unfused"],
                     help="gemv_step is the headline; the others print one extra line per case")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="leave the W4A16 sweep and W8A8 out of the headline line")
+    ap.add_argument("--extra-reps", type=int, default=10,
+                    help="graph replays timed per case of the W4A16 sweep and W8A8")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -722,7 +776,18 @@ def main():
     peak, peak_kind = measured_peaks()
     value = job_throughput(res["step_bytes"], args.steps, world, res["ms"])
     w4_us = statistics.mean(res["w4_us"])
-    achieved = alg_bytes_w4g() / (res["w4_chain_us"] * 1e-6) / 1e9
+    alg = {"w8": alg_bytes_w8(), "w3": alg_bytes_w3(), "w4": alg_bytes_w4g()}
+    kernels = {}
+    for k, t in res["per_kernel"].items():
+        kernels[k] = {"kernel": KERNEL_NAMES[k], "alg_bytes": alg[k],
+                      "us_per_call_chained": t["chained"], "us_per_call_serialized": t["serialized"],
+                      "GBps_chained": alg[k] / (t["chained"] * 1e-6) / 1e9,
+                      "GBps_serialized": alg[k] / (t["serialized"] * 1e-6) / 1e9,
+                      "frac_chained": alg[k] / (t["chained"] * 1e-6) / 1e9 / peak,
+                      "frac_serialized": alg[k] / (t["serialized"] * 1e-6) / 1e9 / peak}
+    # the dominant kernel: the largest share of the step (16 chained launches of each)
+    dom = max(kernels, key=lambda k: kernels[k]["us_per_call_chained"])
+    achieved = kernels[dom]["GBps_chained"]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": True,
@@ -731,21 +796,23 @@ def main():
                    "l2": f"inputs larger than L2: {LAYERS} distinct weight sets, "
                          f"{res['step_bytes'] / 1e6:.0f} MB per step",
                    "us_per_call_mean": res["ms"] / args.steps * 1e3 / (3 * LAYERS),
-                   "w4_actorder_us_per_launch_chained": res["w4_chain_us"],
-                   "w4_actorder_us_per_launch_isolated": w4_us,
+                   "w4_actorder_us_per_launch_in_step": w4_us,
                    "w4_actorder_path": "rows sorted by group once at weight-load time (wq4_actorder_prepare), "
                                        "then wq4_gemm_sorted",
                    "w4_actorder_online_us_per_call": res["w4_online_us"]},
-        "roofline": {"bound": "hbm", "kernel": "k4_gemv_kernel<1,f16,zeros,sorted> (W4 act-order GEMV 4096x11008, "
-                                               "group-sorted rows)",
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES[dom],
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "traffic": K4_SORTED_TRAFFIC_BYTES},
+                     "peak_source": peak_kind, "traffic": TRAFFIC_BYTES[dom],
+                     "launch_time": "average of 16 PDL-chained launches, CUDA events on the launching stream"},
         "e2e": {"value": world * res["step_bytes"] / res["e2e_s_per_step"] / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "steps": res["e2e_steps"]},
         "gpu_launches": 3 * LAYERS * args.steps,
         "clocks": res["clocks"],
     }
+    if not args.no_extra_configs:
+        line["configs"] = {"w4a16_sweep": run_wq4_sweep(args, dev), "w8a8": run_w8a8(args, dev)}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
