@@ -157,33 +157,44 @@ __global__ void __launch_bounds__(kThreads, MP <= 32 ? 2 : 1)  // two CTAs per S
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0 && nst > 0) {
-      prefetch_tensormap(&wmap);
-      prefetch_tensormap(&xmap);
+    // The boxes of a stage are issued by different lanes (lane 0: the packed
+    // weights, lanes 1 ..: the x boxes): on GB300 each issuing thread moves at
+    // most about three million TMA boxes per second (measured), so a single
+    // thread issuing all of them bounded the whole kernel.
+    if (nst > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&wmap);
+        prefetch_tensormap(&xmap);
+      }
       const uint64_t pol = l2_evict_first_policy();
       const uint32_t stage_bytes = kPackedStageBytes + kXStageBytes;
       const int pre = nst < kNS ? nst : kNS;
       // weights of the first stages before the dependency wait, x after it
       for (int i = 0; i < pre; ++i) {
-        mbar_expect_tx(&full[i], stage_bytes);
-        tma_load_2d(sW + size_t(i) * kPackedStageBytes, &wmap, &full[i], n0, (ks0 + i) * (KS / 8), pol);
+        if (lane == 0) mbar_expect_tx(&full[i], stage_bytes);
+        __syncwarp();
+        if (lane == 0) tma_load_2d(sW + size_t(i) * kPackedStageBytes, &wmap, &full[i], n0, (ks0 + i) * (KS / 8), pol);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i)
-#pragma unroll
-        for (int h = 0; h < KS / kBoxK; ++h)
+        if (lane >= 1 && lane <= KS / kBoxK) {
+          const int h = lane - 1;
           tma_load_2d(sX + size_t(i) * kXStageBytes + h * kXBoxBytes, &xmap, &full[i], (ks0 + i) * KS + h * kBoxK, 0, 0ull);
-      for (int i = kNS; i < nst && !*failed; ++i) {
-        const int s = i % kNS;
-        if (!mbar_wait_sleep(&empty[s], ((i / kNS) - 1) & 1)) {
-          *failed = 1;
-          break;
         }
-        mbar_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(sW + size_t(s) * kPackedStageBytes, &wmap, &full[s], n0, (ks0 + i) * (KS / 8), pol);
-#pragma unroll
-        for (int h = 0; h < KS / kBoxK; ++h)
+      for (int i = kNS; i < nst; ++i) {
+        const int s = i % kNS;
+        if (lane == 0) {
+          if (*failed || !mbar_wait_sleep(&empty[s], ((i / kNS) - 1) & 1)) *failed = 1;
+          else mbar_expect_tx(&full[s], stage_bytes);
+        }
+        __syncwarp();
+        if (*failed) break;
+        if (lane == 0) {
+          tma_load_2d(sW + size_t(s) * kPackedStageBytes, &wmap, &full[s], n0, (ks0 + i) * (KS / 8), pol);
+        } else if (lane <= KS / kBoxK) {
+          const int h = lane - 1;
           tma_load_2d(sX + size_t(s) * kXStageBytes + h * kXBoxBytes, &xmap, &full[s], (ks0 + i) * KS + h * kBoxK, 0, 0ull);
+        }
       }
     } else {
       pdl_wait();

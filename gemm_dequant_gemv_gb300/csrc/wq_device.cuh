@@ -191,6 +191,15 @@ __device__ __forceinline__ uint32_t shf_r(uint32_t lo, uint32_t hi, uint32_t n) 
 }
 __device__ __forceinline__ float as_f32(uint32_t u) { return __uint_as_float(u); }
 
+// (a & b) | c as one logic instruction.  Written in C++ the compiler emits an
+// AND and an OR (measured on GB300: about 1.85 logic instructions per use),
+// and the logic pipe is what the GEMV inner loops run out of first.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));

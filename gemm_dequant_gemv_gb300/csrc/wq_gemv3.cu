@@ -178,8 +178,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             const int j = 2 * jp + h;
             const uint32_t mask = 7u << code_offset(j);
             const int src = code_src(j);
-            const float2 m01 = make_float2(as_f32((t[0][src] & mask) | magic), as_f32((t[1][src] & mask) | magic));
-            const float2 m23 = make_float2(as_f32((t[2][src] & mask) | magic), as_f32((t[3][src] & mask) | magic));
+            const float2 m01 = make_float2(as_f32(lop3_and_or(t[0][src], mask, magic)),
+                                           as_f32(lop3_and_or(t[1][src], mask, magic)));
+            const float2 m23 = make_float2(as_f32(lop3_and_or(t[2][src], mask, magic)),
+                                           as_f32(lop3_and_or(t[3][src], mask, magic)));
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               const float2 xp = h ? make_float2(xq[m].z, xq[m].w) : make_float2(xq[m].x, xq[m].y);

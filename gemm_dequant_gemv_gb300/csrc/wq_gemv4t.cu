@@ -77,6 +77,7 @@ static_assert(kWarpK == 256 && kStageK == 512, "one 256-value TMA box of x per c
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 __host__ __device__ inline size_t align1k(size_t v) { return (v + 1023) & ~size_t(1023); }
+__host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~size_t(127); }
 
 struct Smem4T {
   size_t ring, xst, xg, pv, scl, zp, recv, bars, flag, total;
@@ -87,11 +88,11 @@ struct Smem4T {
     ring = o;  o = align1k(o + size_t(NS) * nslab * kSlabStageBytes);
     xst = o;   o = align16(o + (perm ? 0 : size_t(NS) * xstage_bytes(MT)));
     xg = o;    o = align16(o + (perm ? size_t(MT + 1) * krange * 2 : 0));
-    pv = o;    o = align16(o + (perm ? size_t(krange) * 4 : 0));
-    scl = o;   o = align16(o + size_t(ng_max) * nslab * kSlabCols * 2);
+    pv = o;    o = align128(o + (perm ? size_t(krange) * 4 : 0));
+    scl = o;   o = align128(o + size_t(ng_max) * nslab * kSlabCols * 2);    // TMA destinations: 128-byte aligned
     zp = o;    o = align16(o + size_t(ng_max) * nslab * (kSlabCols / 8) * 4);
     recv = o;  o = align16(o + size_t(S) * kKW * nown * MT * kSlabCols * 4);
-    bars = o;  o = align16(o + size_t(2 * NS + 2) * 8);
+    bars = o;  o = align16(o + size_t(2 * NS + 3) * 8);
     flag = o;  o = align16(o + 16);
     total = o;
   }
@@ -111,21 +112,13 @@ struct Args4T {
   int MT, nslab, NS, ng_max;
   int gshift;              // log2(units per group)
   int krange;              // values of k of the largest K-slice (multiple of 64)
+  int tma_tables;          // scales (and zeros) of the CTA's groups by one TMA box each
 };
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 __device__ __forceinline__ __nv_bfloat162 as_b2(uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); }
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 __device__ __forceinline__ uint32_t b2_bits(__nv_bfloat162 h) { return *reinterpret_cast<const uint32_t*>(&h); }
-
-// (a & b) | c as ONE logic instruction.  Written in C++ the compiler emits an
-// AND and an OR here (measured on GB300: 1.85 logic instructions per use);
-// the logic pipe is this kernel's limit, so the fusion is spelled out.
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
 
 // Code pair PI of a packed word as q - z: PI = 0: codes (0, 4), 1: (1, 5),
 // 2: (2, 6), 3: (3, 7) in the (low, high) halves.  zsub = pair of -(1024 + z)
@@ -171,10 +164,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 
+// Act-order instances (short K-slices, chained in a decode step) are sized for
+// two CTAs per SM, so that the next launch's CTAs can start, read their tables
+// and prefetch their weights beside this launch's.
+constexpr int kMaxSlabsPerm = 5;
 template <int ACT_BF16, bool HAS_Z, bool PERM, bool TILED>
-__global__ void __launch_bounds__(17 * 32, 1)
+__global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32, PERM ? 2 : 1)
     k4t_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap8,
-                    const __grid_constant__ CUtensorMap xmap, const Args4T a) {
+                    const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
+                    const __grid_constant__ CUtensorMap zmap, const Args4T a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int S = gridDim.x;
   const int nslab = a.nslab, NS = a.NS, MT = a.MT;
@@ -192,6 +190,7 @@ __global__ void __launch_bounds__(17 * 32, 1)
   uint64_t* empty = full + NS;
   uint64_t* recv_bar = empty + NS;
   uint64_t* pbar = recv_bar + 1;  // the perm slice (act-order)
+  uint64_t* tbar = pbar + 1;      // the scale and zero tables
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L.flag);  // producer's
   volatile int* cfailed = failed + 1;                                       // consumers'
 
@@ -219,6 +218,7 @@ __global__ void __launch_bounds__(17 * 32, 1)
       mbar_init(&empty[s], W);
     }
     mbar_init(pbar, 1);
+    mbar_init(tbar, 1);
     *failed = 0;
     *cfailed = 0;
     if (S == 1) {
@@ -273,6 +273,12 @@ __global__ void __launch_bounds__(17 * 32, 1)
                       l2_evict_first_policy());
       }
     };
+    const uint32_t tbytes = uint32_t(a.ng_max) * BN * 2 + (HAS_Z ? uint32_t(a.ng_max) * (BN / 8) * 4 : 0u);
+    if (a.tma_tables && lane == 0 && u1 > u0) {  // this CTA's scale (and zero) rows: one box each
+      mbar_expect_tx(tbar, tbytes);
+      tma_load_2d(scl, &smap, tbar, n0, g0, 0ull);
+      if (HAS_Z) tma_load_2d(zp, &zmap, tbar, n0 / 8, g0, 0ull);
+    }
     if (PERM && lane == 0 && u1 > u0) {  // the perm slice is weight-side data: before the dependency wait
       mbar_expect_tx(pbar, uint32_t(u1 - u0) * kUnitK * 4);
       bulk_load(smem + L.pv, a.perm + kUnitK * u0, uint32_t(u1 - u0) * kUnitK * 4, pbar);
@@ -317,7 +323,8 @@ __global__ void __launch_bounds__(17 * 32, 1)
     }
     if (lane == 0 && *failed) {
       drain_stages_rt(full, NS, issued);
-      if (PERM && u1 > u0) mbar_wait(pbar, 0);  // the perm copy lands before the shared memory goes away
+      if (PERM && u1 > u0) mbar_wait(pbar, 0);  // the copies land before the shared memory goes away
+      if (a.tma_tables && u1 > u0) mbar_wait(tbar, 0);
     }
     __syncwarp();
     if (S > 1) cluster_wait();
@@ -325,21 +332,42 @@ __global__ void __launch_bounds__(17 * 32, 1)
     // ----------------------------------------------------------------- consumers
     const int tid = threadIdx.x;
     const int nthr = W * 32;
-    // weight-side tables of this CTA's groups, read before the dependency wait:
-    // scl[g][c] = raw 16-bit scale, zp[g][c/8] = raw packed zeros (8 per word)
-    {
+    // weight-side tables of this CTA's groups: scl[g][c] = raw 16-bit scale,
+    // zp[g][c/8] = raw packed zeros (8 per word).  Normally one TMA box each,
+    // issued by the producer at the start; where the zeros' row pitch rules a
+    // box out, read here before the dependency wait, four loads in flight per
+    // thread (a load-store loop would wait out one memory latency per element)
+    if (!a.tma_tables) {
       const uint16_t* SC = static_cast<const uint16_t*>(a.scales);
-      for (int i = tid; i < ng * (BN / 2); i += nthr) {
-        const int gr = i / (BN / 2), c = 2 * (i % (BN / 2));
-        uint32_t v = 0;
-        if (n0 + c < N) v = *reinterpret_cast<const uint32_t*>(SC + size_t(g0 + gr) * N + n0 + c);
-        reinterpret_cast<uint32_t*>(scl)[i] = v;
-      }
-      if (HAS_Z)
-        for (int i = tid; i < ng * (BN / 8); i += nthr) {
-          const int gr = i / (BN / 8), c = i % (BN / 8);
-          zp[i] = (n0 + 8 * c < N) ? static_cast<uint32_t>(a.qzeros[size_t(g0 + gr) * (N / 8) + n0 / 8 + c]) : 0u;
+      const int ns = ng * (BN / 2);
+      for (int i0 = tid; i0 < ns; i0 += 4 * nthr) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * nthr, gr = i / (BN / 2), c = 2 * (i % (BN / 2));
+          v[j] = (i < ns && n0 + c < N) ? *reinterpret_cast<const uint32_t*>(SC + size_t(g0 + gr) * N + n0 + c) : 0u;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (i0 + j * nthr < ns) reinterpret_cast<uint32_t*>(scl)[i0 + j * nthr] = v[j];
+      }
+      if (HAS_Z) {
+        const int nz = ng * (BN / 8);
+        for (int i0 = tid; i0 < nz; i0 += 4 * nthr) {
+          uint32_t v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nthr, gr = i / (BN / 8), c = i % (BN / 8);
+            v[j] = (i < nz && n0 + 8 * c < N)
+                       ? static_cast<uint32_t>(a.qzeros[size_t(g0 + gr) * (N / 8) + n0 / 8 + c]) : 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i0 + j * nthr < nz) zp[i0 + j * nthr] = v[j];
+        }
+      }
+    }
+    {
       if (!PERM)  // the zero row after each 256-value half of every x stage
         for (int i = tid; i < NS * 2 * 128; i += nthr) {
           const int st = i / 256, h = (i / 128) % 2, c = i % 128;
@@ -378,6 +406,7 @@ __global__ void __launch_bounds__(17 * 32, 1)
       }
     }
     consumer_sync(nthr);  // tables (and the gathered x) complete before any warp uses them
+    if (a.tma_tables && u1 > u0 && !mbar_wait(tbar, 0)) *cfailed = 1;
 
     const int g = lane >> 2, t = lane & 3;
     const int slab = warp / kKW, kpart = warp % kKW;
@@ -615,7 +644,7 @@ cudaError_t launch_4t(const Problem4T& pr) {
   struct Cand { long long cost; int S, nslab; };
   Cand cands[5 * 8];
   int nc = 0;
-  for (int nslab = 4; nslab <= 8; ++nslab)
+  for (int nslab = 4; nslab <= (PERM ? kMaxSlabsPerm : 8); ++nslab)
     for (int S = 1; S <= 8 && S <= units; ++S)
       cands[nc++] = Cand{static_cast<long long>(nslab) * ((units + S - 1) / S), S, nslab};
   std::sort(cands, cands + nc, [](const Cand& a, const Cand& b) {
@@ -630,9 +659,10 @@ cudaError_t launch_4t(const Problem4T& pr) {
     if (T * S > device_sm_count()) continue;
     const int ng = groups_per_slice_max(units, S, pr.group);
     const int kr = krange_max(units, S);
-    // short K-slices (at most four stages): a two-stage ring, so that the next
-    // kernel's CTA fits on the SM beside this one and prefetches its weights
-    int NS = kr <= 4 * kStageK ? 2 : 3;
+    // a three-stage ring; its shared memory (over half an SM's) also keeps two
+    // CTAs of one launch off the same SM, while the CTA of a smaller kernel
+    // launched next can still start beside it
+    int NS = 3;
     size_t sm = Smem4T(nslab, NS, MT, S, ng, PERM, kr).total;
     while (sm > static_cast<size_t>(max_smem) && NS > 2) sm = Smem4T(nslab, --NS, MT, S, ng, PERM, kr).total;
     if (sm > static_cast<size_t>(max_smem)) continue;
@@ -669,8 +699,22 @@ cudaError_t launch_4t(const Problem4T& pr) {
   if (!PERM && !encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, pr.x, pr.K, pr.M, size_t(pr.K) * 2, 256,
                                      MT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  // scale rows [K/group, N] (16-bit) and packed zero rows [K/group, N/8] (int32): one
+  // box of ng_max rows each per CTA; the zeros' row pitch (N/2 bytes) must be a
+  // multiple of 16 and the scale box at most 256 rows
+  CUtensorMap smap, zmap;
+  memset(&smap, 0, sizeof smap);
+  memset(&zmap, 0, sizeof zmap);
+  const int G = pr.K / pr.group;
+  bool tma_tables = ng_max <= 256 && (!HZ || (pr.N / 2) % 16 == 0);
+  if (tma_tables)
+    tma_tables = encode_tensor_map_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, pr.scales, pr.N, G, size_t(pr.N) * 2,
+                                      q.nslab * kSlabCols, ng_max, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 (!HZ || encode_tensor_map_2d(&zmap, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, pr.N / 8, G,
+                                              size_t(pr.N / 8) * 4, q.nslab * kSlabCols / 8, ng_max,
+                                              CU_TENSOR_MAP_SWIZZLE_NONE));
   Args4T a{pr.x, pr.y, pr.scales, pr.qzeros, pr.wtiled, pr.perm, pr.M, pr.K, pr.N, pr.group, MT, q.nslab, q.NS,
-           ng_max, pr.gshift, krange_max(units, q.S)};
+           ng_max, pr.gshift, krange_max(units, q.S), tma_tables ? 1 : 0};
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -694,7 +738,7 @@ cudaError_t launch_4t(const Problem4T& pr) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  void* args[4] = {&wmap, &wmap8, &xmap, &a};
+  void* args[6] = {&wmap, &wmap8, &xmap, &smap, &zmap, &a};
   return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
