@@ -70,9 +70,10 @@ constexpr int kUnitBytes = kSlabCols * (kUnitK / 8) * 4;  // 1 KB
 constexpr int kStageUnits = 8;
 constexpr int kStageK = kStageUnits * kUnitK;            // 512
 constexpr int kSlabStageBytes = kStageUnits * kUnitBytes;  // 8 KB
-constexpr int kKW = 2;                                   // consumer warps per slab
-constexpr int kUnitsPerWarp = kStageUnits / kKW;         // 4
-constexpr int kWarpK = kUnitsPerWarp * kUnitK;           // 256 values of k per warp and stage
+constexpr int kKW = 2;                                   // consumer warps per slab (x staged per stage)
+constexpr int kKWPerm = 4;                               // consumer warps per slab (act-order, gathered x)
+__host__ __device__ constexpr int kw_of(bool perm) { return perm ? kKWPerm : kKW; }
+constexpr int kWarpK = kStageUnits / kKW * kUnitK;       // 256 values of k per warp and stage
 static_assert(kWarpK == 256 && kStageK == 512, "one 256-value TMA box of x per consumer warp's half of a stage");
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -91,7 +92,7 @@ struct Smem4T {
     pv = o;    o = align128(o + (perm ? size_t(krange) * 4 : 0));
     scl = o;   o = align128(o + size_t(ng_max) * nslab * kSlabCols * 2);    // TMA destinations: 128-byte aligned
     zp = o;    o = align16(o + size_t(ng_max) * nslab * (kSlabCols / 8) * 4);
-    recv = o;  o = align16(o + size_t(S) * kKW * nown * MT * kSlabCols * 4);
+    recv = o;  o = align16(o + size_t(S) * kw_of(perm) * nown * MT * kSlabCols * 4);
     bars = o;  o = align16(o + size_t(2 * NS + 3) * 8);
     flag = o;  o = align16(o + 16);
     total = o;
@@ -164,19 +165,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 
-// Act-order instances (short K-slices, chained in a decode step) are sized for
-// two CTAs per SM, so that the next launch's CTAs can start, read their tables
-// and prefetch their weights beside this launch's.
+// Act-order instances (short K-slices, chained in a decode step) run four
+// consumer warps per slab: more warps in flight for the latency of the
+// conversion and MMA chains of a short slice.
 constexpr int kMaxSlabsPerm = 5;
 template <int ACT_BF16, bool HAS_Z, bool PERM, bool TILED>
-__global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32, PERM ? 2 : 1)
+__global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17 * 32, 1)
     k4t_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap8,
                     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                     const __grid_constant__ CUtensorMap zmap, const Args4T a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int S = gridDim.x;
   const int nslab = a.nslab, NS = a.NS, MT = a.MT;
-  const int W = nslab * kKW;  // consumer warps
+  constexpr int KW = kw_of(PERM), UPW = kStageUnits / KW;  // warps per slab, units per warp and stage
+  const int W = nslab * KW;  // consumer warps
   const Smem4T L(nslab, NS, MT, S, a.ng_max, PERM, a.krange);
   uint8_t* ring = smem + L.ring;
   uint8_t* xst = smem + L.xst;
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
       mbar_init(recv_bar, W * 32);
     } else {
       mbar_init(recv_bar, 1);
-      const uint32_t rb = uint32_t(S) * kKW * nown * MT * kSlabCols * 4;
+      const uint32_t rb = uint32_t(S) * KW * nown * MT * kSlabCols * 4;
       if (rb) mbar_expect_tx(recv_bar, rb);
     }
     fence_mbar_init();
@@ -400,8 +402,13 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
             v[j] = i < kr ? Xm[min(max(pvs[i], 0), K - 1)] : 0;  // clamped: never read out of bounds
           }
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (i0 + j * nthr < kr) xg[size_t(m) * krp + i0 + j * nthr] = v[j];
+          for (int j = 0; j < 4; ++j) {
+            // stored in the MMA's pair order: within each 8 values of k, (x0, x4),
+            // (x1, x5), (x2, x6), (x3, x7) -- one 16-byte load per word row then
+            // gives the four B registers without any byte permutes
+            const int i = i0 + j * nthr;
+            if (i < kr) xg[size_t(m) * krp + (i & ~7) + 2 * (i & 3) + ((i >> 2) & 1)] = v[j];
+          }
         }
       }
     }
@@ -409,11 +416,11 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
     if (a.tma_tables && u1 > u0 && !mbar_wait(tbar, 0)) *cfailed = 1;
 
     const int g = lane >> 2, t = lane & 3;
-    const int slab = warp / kKW, kpart = warp % kKW;
+    const int slab = warp / KW, kpart = warp % KW;
     const int col4 = slab * kSlabCols + 4 * g;  // this thread's 4 columns within the tile
     const bool slab_live = !TILED || slab < nvalid;
     const int xrow = g < MT ? g : MT;  // x row of this lane's B fragment (MT: the zero row)
-    const int ub = kpart * kUnitsPerWarp;  // first unit of this warp within a stage
+    const int ub = kpart * UPW;  // first unit of this warp within a stage
 
     // acc: running sums (scale applied); tmp: the current group's MMA sums
     float acc[2][4], tmp[2][4];
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
       const uint8_t* wst = ring + size_t(s) * stage_w;
       if (slab_live) {
 #pragma unroll
-        for (int uu = 0; uu < kUnitsPerWarp; ++uu) {
+        for (int uu = 0; uu < UPW; ++uu) {
           const int ul = ub + uu;  // unit within the stage
           if (ul >= nu) break;
           const int u = u0 + kStageUnits * it + ul;
@@ -489,8 +496,10 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
             const uint4 wv = TILED ? *reinterpret_cast<const uint4*>(ublk + ab * 512 + lane * 16)
                                    : *reinterpret_cast<const uint4*>(ublk + rr * 128 + (((g ^ rr) & 7) << 4));
             const uint4 xv = *reinterpret_cast<const uint4*>(xu + rr * 16);
-            const uint32_t b0 = prmt(xv.x, xv.z, 0x5410u), b1 = prmt(xv.x, xv.z, 0x7632u);
-            const uint32_t b2 = prmt(xv.y, xv.w, 0x5410u), b3 = prmt(xv.y, xv.w, 0x7632u);
+            // B registers: the x pairs (x0, x4), (x1, x5), (x2, x6), (x3, x7) of the word row
+            // (the gathered act-order x is stored in that order already)
+            const uint32_t b0 = PERM ? xv.x : prmt(xv.x, xv.z, 0x5410u), b1 = PERM ? xv.y : prmt(xv.x, xv.z, 0x7632u);
+            const uint32_t b2 = PERM ? xv.z : prmt(xv.y, xv.w, 0x5410u), b3 = PERM ? xv.w : prmt(xv.y, xv.w, 0x7632u);
             const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
             for (int tl = 0; tl < 2; ++tl) {
@@ -523,7 +532,7 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
     // owner of slab w is cluster rank w % S, slot (sender, kpart, w / S, m)
     const int owner = slab % S, lslab = slab / S;
     auto slot = [&](int sender, int m) {
-      return recv + ((size_t(sender * kKW + kpart) * nown_max + lslab) * MT + m) * kSlabCols + 4 * g;
+      return recv + ((size_t(sender * KW + kpart) * nown_max + lslab) * MT + m) * kSlabCols + 4 * g;
     };
     if (S == 1) {
 #pragma unroll
@@ -555,8 +564,8 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * 2 + 1) * 32 : 17 * 32,
       const int n = n0 + (int(rank) + S * i) * kSlabCols + c;
       float v = 0.f;
       for (int sender = 0; sender < S; ++sender)
-        for (int j = 0; j < kKW; ++j)
-          v += recv[((size_t(sender * kKW + j) * nown_max + i) * MT + m) * kSlabCols + c];
+        for (int j = 0; j < KW; ++j)
+          v += recv[((size_t(sender * KW + j) * nown_max + i) * MT + m) * kSlabCols + c];
       if (n < N) Y[size_t(m) * N + n] = f32_to_act<ACT_BF16>(v);
     }
   }
@@ -666,7 +675,7 @@ cudaError_t launch_4t(const Problem4T& pr) {
     size_t sm = Smem4T(nslab, NS, MT, S, ng, PERM, kr).total;
     while (sm > static_cast<size_t>(max_smem) && NS > 2) sm = Smem4T(nslab, --NS, MT, S, ng, PERM, kr).total;
     if (sm > static_cast<size_t>(max_smem)) continue;
-    const int threads = (nslab * kKW + 1) * 32;
+    const int threads = (nslab * kw_of(PERM) + 1) * 32;
     // capacity counted at one CTA per SM (planning smem above half an SM's)
     if (T > cluster_capacity(kern, S, threads, std::max(sm, static_cast<size_t>(max_smem) / 2 + 1024))) continue;
     q = Plan4T{nslab, S, T, NS, MT};
@@ -684,7 +693,7 @@ cudaError_t launch_4t(const Problem4T& pr) {
     smem = sm;
     ng_max = ng;
   }
-  const int threads = (q.nslab * kKW + 1) * 32;
+  const int threads = (q.nslab * kw_of(PERM) + 1) * 32;
   CUtensorMap wmap, wmap8, xmap;
   memset(&wmap, 0, sizeof wmap);
   memset(&wmap8, 0, sizeof wmap8);
