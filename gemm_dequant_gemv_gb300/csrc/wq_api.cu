@@ -4,7 +4,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/wq.h"
 #include "wq_gemv_common.cuh"
@@ -65,6 +67,49 @@ int device_max_smem() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Clusters of S CTAs (threads, smem each) the device runs at once, per
+// kernel instance and configuration; looked up once and cached (the only
+// process-wide state besides the tensor-map encoder, guarded by a mutex).
+int cluster_capacity(const void* kern, int S, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, int, size_t>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(dev, kern, S, threads, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  if (S == 1) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess) return 0;
+    n = per_sm * device_sm_count();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // an unsupported cluster shape: report no capacity
+      n = 0;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
   return n;
 }
 
@@ -221,6 +266,13 @@ WQ_API wq_status wq3_gemv(const void* x, const int32_t* mat, const void* scales,
   if (!aligned16(x) || !aligned16(mat) || !aligned16(scales) || !aligned16(zeros) || !aligned16(y))
     return WQ_ERR_ALIGN;
 
+  // M >= 3: the tensor-core kernel (its MMAs cost the same for any M <= 8),
+  // where its pair-ordered x fits in shared memory; M <= 2 and the rest: the
+  // CUDA-core kernel (faster there: 5.0 against 5.4 us at M = 1, chained)
+  if (M >= 3) {
+    const cudaError_t e = launch_wq3t(x, mat, scales, zeros, y, M, K, N, flags, static_cast<cudaStream_t>(stream));
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
   const int T = (N + 127) / 128, units = K / 32;
   LaunchPlan p{T, plan_splits(T, units), round_mt(M), flags, static_cast<cudaStream_t>(stream)};
   GemvArgs a{x, y, scales, zeros, nullptr, M, K, N, 0, 0};

@@ -571,49 +571,6 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17
   }
 }
 
-// Clusters of S CTAs (threads, smem each) the device runs at once, per
-// kernel instance and configuration; looked up once and cached (the only
-// process-wide state of this file, guarded by a mutex).
-int cluster_capacity(const void* kern, int S, int threads, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int, int, size_t>, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const auto key = std::make_tuple(dev, kern, S, threads, smem);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-  }
-  int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return 0;
-  if (S == 1) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess) return 0;
-    n = per_sm * device_sm_count();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = S;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-      cudaGetLastError();  // an unsupported cluster shape: report no capacity
-      n = 0;
-    }
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  cache[key] = n;
-  return n;
-}
-
 struct Problem4T {
   const void* x;
   const int32_t* qweight;

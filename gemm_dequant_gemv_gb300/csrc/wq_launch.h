@@ -68,8 +68,18 @@ cudaError_t launch_wq4t(const void* x, const int32_t* qweight, const uint8_t* wt
                         const int32_t* qzeros, const int32_t* perm, void* y, int M, int K, int N, int group,
                         int act_bf16, unsigned flags, cudaStream_t stream);
 
+// 3-bit GEMV with per-column scale and stored zero on the warp-level
+// tensor-core MMA (wq_gemv3t.cu), planned per call.  cudaErrorNotSupported
+// for shapes it does not take (M > 8, K % 32, N % 8, shared memory).
+cudaError_t launch_wq3t(const void* x, const int32_t* mat, const void* scales, const void* zeros, void* y, int M,
+                        int K, int N, unsigned flags, cudaStream_t stream);
+
 // Device queries and tensor-map encoding (wq_api.cu).
 int device_sm_count();
+// Clusters of S CTAs of `threads` threads and `smem` bytes of dynamic shared
+// memory each that the device runs at once for kernel `kern` (S == 1: CTAs);
+// cached per device and configuration, 0 for a shape the device cannot run.
+int cluster_capacity(const void* kern, int S, int threads, size_t smem);
 int device_max_smem();
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,

@@ -72,6 +72,31 @@ def test_wq3_parity(G, M, K, N):
     _tol(G.to_f64(y), y_ref, a, "f16")
 
 
+# shapes that steer the 3-bit tensor-core kernel (M >= 3) and its plan: K not
+# a multiple of the 128-value unit, N not a multiple of the 32-column slab, M
+# between the MMA rows; K-slices over a cluster (small N, long K); column tiles
+# in several waves (N beyond what one wave holds); and a pair-ordered x too
+# large for shared memory (M = 8 at very long K), which goes to the CUDA-core
+# kernel like every M <= 2
+WQ3T_CASES = [(5, 96, 264), (7, 1056, 1000), (3, 4128, 520), (4, 16384, 256), (8, 16384, 256),
+              (3, 64, 40960), (8, 131072, 64), (2, 4128, 520)]
+
+
+@pytest.mark.parametrize("M,K,N", WQ3T_CASES)
+def test_wq3_plan_shapes(G, M, K, N):
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq3(seed=4, M=M, K=K, N=N)
+    y = G.to_f64(G.run_wq3(d))
+    cols = None
+    if N > 4096:
+        r = np.random.default_rng(6)
+        cols = np.unique(np.concatenate([np.arange(0, 256), np.arange(N - 256, N), r.integers(0, N, 512)]))
+    y_ref, a = oracle.wq3_gemv(d["x"].view(np.uint16), d["mat"], d["scales"].view(np.uint16),
+                               d["zeros"].view(np.uint16), cols=cols)
+    _tol(y if cols is None else y[:, cols], y_ref, a, "f16")
+
+
 W3_ADV_CASES = [(1, 4096, 4096, "same"), (8, 4096, 512, "same"), (1, 16384, 20480, "same"),
                 (8, 16384, 1024, "same"), (1, 4096, 4096, "halves"), (1, 16384, 20480, "halves")]
 
