@@ -301,6 +301,14 @@ WQ_API wq_status wq4_gemm(const void* x, const int32_t* qweight, const void* sca
 
   if (M > 8) {
     if (g_idx) return WQ_ERR_UNSUPPORTED;
+    // up to 32 rows: the warp-level MMA kernel with two or four n-tiles (the
+    // conversion of each code serves every row, and it measured about twice
+    // as fast as the tcgen05 kernel there); beyond, the tcgen05 kernel
+    if (M <= 32 && K % wq4t_unit_k() == 0 && group_size % wq4t_unit_k() == 0) {
+      const cudaError_t e = launch_wq4t(x, qweight, nullptr, scales, qzeros, nullptr, y, M, K, N, group_size,
+                                        act_bf16, flags, static_cast<cudaStream_t>(stream));
+      if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
     return from_cuda(launch_wq4_mma(x, qweight, scales, qzeros, y, M, K, N, group_size, act_bf16, flags,
                                     static_cast<cudaStream_t>(stream)));
   }

@@ -384,7 +384,8 @@ __global__ void __maxnreg__(kMaxRegs3) k3t_gemv_kernel(const Args3T a) {
   // ---------------------------------------------- owner: sum the pieces, store y
   // the S * KW pieces of an element are added by `lanes` neighbouring lanes
   // (a power of two up to 16), then in a fixed butterfly order
-  if (nown > 0 && mbar_wait(recv_bar, 0)) {
+  // (every lane of a warp takes the same branch: the butterfly needs the whole warp)
+  if (__all_sync(0xffffffffu, nown > 0 && mbar_wait(recv_bar, 0))) {
     __half* Y = static_cast<__half*>(a.y);
     const int npieces = S * KW, per = M * kSlabCols;
     int lanes = 1;

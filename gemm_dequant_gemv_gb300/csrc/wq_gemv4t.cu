@@ -92,7 +92,14 @@ struct Smem4T {
     pv = o;    o = align128(o + (perm ? size_t(krange) * 4 : 0));
     scl = o;   o = align128(o + size_t(ng_max) * nslab * kSlabCols * 2);    // TMA destinations: 128-byte aligned
     zp = o;    o = align16(o + size_t(ng_max) * nslab * (kSlabCols / 8) * 4);
-    recv = o;  o = align16(o + size_t(S) * kw_of(perm) * nown * MT * kSlabCols * 4);
+    // the partial sums: without a cluster (S == 1) they reuse the ring, which
+    // every consumer has finished with by then (it holds at least two stages:
+    // nslab * 16 KB >= the KW * nslab * MT * 128 bytes of pieces for MT <= 32)
+    if (S == 1) {
+      recv = ring;
+    } else {
+      recv = o;  o = align16(o + size_t(S) * kw_of(perm) * nown * MT * kSlabCols * 4);
+    }
     bars = o;  o = align16(o + size_t(2 * NS + 3) * 8);
     flag = o;  o = align16(o + 16);
     total = o;
@@ -169,8 +176,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // consumer warps per slab: more warps in flight for the latency of the
 // conversion and MMA chains of a short slice.
 constexpr int kMaxSlabsPerm = 5;
-template <int ACT_BF16, bool HAS_Z, bool PERM, bool TILED>
-__global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17 * 32, 1)
+// NT: 8-row n-tiles of the MMA (rows of x: NT = 1 up to 8, 2 up to 16, 4 up
+// to 32); the converted A fragments serve every n-tile.
+template <int ACT_BF16, bool HAS_Z, bool PERM, bool TILED, int NT>
+__global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : (NT == 4 ? 13 : 17) * 32, 1)
     k4t_gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap8,
                     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                     const __grid_constant__ CUtensorMap zmap, const Args4T a) {
@@ -419,15 +428,19 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17
     const int slab = warp / KW, kpart = warp % KW;
     const int col4 = slab * kSlabCols + 4 * g;  // this thread's 4 columns within the tile
     const bool slab_live = !TILED || slab < nvalid;
-    const int xrow = g < MT ? g : MT;  // x row of this lane's B fragment (MT: the zero row)
+    // x row of this lane's B fragment in n-tile nt (MT: the zero row; with
+    // several n-tiles MT = 8 NT and rows past M are TMA zero fill)
+    const int xrow = g < MT ? g : MT;
     const int ub = kpart * UPW;  // first unit of this warp within a stage
 
     // acc: running sums (scale applied); tmp: the current group's MMA sums
-    float acc[2][4], tmp[2][4];
+    float acc[2][NT][4], tmp[2][NT][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[j][i] = tmp[j][i] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][nt][i] = tmp[j][nt][i] = 0.f;
     int cur_g = -1;
     // per column of the thread: pair of -(1024 + z) (fp16) or -(128 + z) (bf16),
     // and (fp16) pair of -(64 + z); z = 8 without stored zeros
@@ -447,10 +460,12 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17
 #pragma unroll
       for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[tl][i] = fmaf(sv[2 * tl + (i >> 1)], tmp[tl][i], acc[tl][i]);
-          tmp[tl][i] = 0.f;
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[tl][nt][i] = fmaf(sv[2 * tl + (i >> 1)], tmp[tl][nt][i], acc[tl][nt][i]);
+            tmp[tl][nt][i] = 0.f;
+          }
     };
 
     int s = 0;
@@ -495,25 +510,33 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17
             const int rr = 2 * t + ab;  // word row within the unit
             const uint4 wv = TILED ? *reinterpret_cast<const uint4*>(ublk + ab * 512 + lane * 16)
                                    : *reinterpret_cast<const uint4*>(ublk + rr * 128 + (((g ^ rr) & 7) << 4));
-            const uint4 xv = *reinterpret_cast<const uint4*>(xu + rr * 16);
-            // B registers: the x pairs (x0, x4), (x1, x5), (x2, x6), (x3, x7) of the word row
-            // (the gathered act-order x is stored in that order already)
-            const uint32_t b0 = PERM ? xv.x : prmt(xv.x, xv.z, 0x5410u), b1 = PERM ? xv.y : prmt(xv.x, xv.z, 0x7632u);
-            const uint32_t b2 = PERM ? xv.z : prmt(xv.y, xv.w, 0x5410u), b3 = PERM ? xv.w : prmt(xv.y, xv.w, 0x7632u);
+            // B registers of each n-tile: the x pairs (x0, x4), (x1, x5), (x2, x6),
+            // (x3, x7) of the word row (the gathered act-order x is stored in that
+            // order already); n-tile nt reads row 8 nt + g, 16 * 256 bytes further on
+            uint32_t bx[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xu + rr * 16 + nt * (8 * 256 * 2));
+              bx[nt][0] = PERM ? xv.x : prmt(xv.x, xv.z, 0x5410u);
+              bx[nt][1] = PERM ? xv.y : prmt(xv.x, xv.z, 0x7632u);
+              bx[nt][2] = PERM ? xv.z : prmt(xv.y, xv.w, 0x5410u);
+              bx[nt][3] = PERM ? xv.w : prmt(xv.y, xv.w, 0x7632u);
+            }
             const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
             for (int tl = 0; tl < 2; ++tl) {
               const uint32_t we = w4[2 * tl], wo = w4[2 * tl + 1];
               const uint32_t we8 = we >> 8, wo8 = wo >> 8;
               const uint32_t zse = zsv[2 * tl], zso = zsv[2 * tl + 1], zfe = zfv[2 * tl], zfo = zfv[2 * tl + 1];
-              mma_16816<ACT_BF16>(tmp[tl], convert_pair<ACT_BF16, 0>(we, we8, zse, zfe),
-                                  convert_pair<ACT_BF16, 0>(wo, wo8, zso, zfo),
-                                  convert_pair<ACT_BF16, 1>(we, we8, zse, zfe),
-                                  convert_pair<ACT_BF16, 1>(wo, wo8, zso, zfo), b0, b1);
-              mma_16816<ACT_BF16>(tmp[tl], convert_pair<ACT_BF16, 2>(we, we8, zse, zfe),
-                                  convert_pair<ACT_BF16, 2>(wo, wo8, zso, zfo),
-                                  convert_pair<ACT_BF16, 3>(we, we8, zse, zfe),
-                                  convert_pair<ACT_BF16, 3>(wo, wo8, zso, zfo), b2, b3);
+              const uint32_t q0 = convert_pair<ACT_BF16, 0>(we, we8, zse, zfe), q1 = convert_pair<ACT_BF16, 0>(wo, wo8, zso, zfo);
+              const uint32_t q2 = convert_pair<ACT_BF16, 1>(we, we8, zse, zfe), q3 = convert_pair<ACT_BF16, 1>(wo, wo8, zso, zfo);
+              const uint32_t q4 = convert_pair<ACT_BF16, 2>(we, we8, zse, zfe), q5 = convert_pair<ACT_BF16, 2>(wo, wo8, zso, zfo);
+              const uint32_t q6 = convert_pair<ACT_BF16, 3>(we, we8, zse, zfe), q7 = convert_pair<ACT_BF16, 3>(wo, wo8, zso, zfo);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_16816<ACT_BF16>(tmp[tl][nt], q0, q1, q2, q3, bx[nt][0], bx[nt][1]);
+                mma_16816<ACT_BF16>(tmp[tl][nt], q4, q5, q6, q7, bx[nt][2], bx[nt][3]);
+              }
             }
           }
         }
@@ -528,30 +551,36 @@ __global__ void __launch_bounds__(PERM ? (kMaxSlabsPerm * kKWPerm + 1) * 32 : 17
     if (cur_g >= 0) fold(cur_g);
 
     // ------------------------------------------------ split-K partial sums out
-    // this thread holds rows m = 2t, 2t+1 of columns col4 .. col4 + 3; the
-    // owner of slab w is cluster rank w % S, slot (sender, kpart, w / S, m)
+    // this thread holds rows m = 8 nt + 2t, 8 nt + 2t + 1 of columns col4 ..
+    // col4 + 3; the owner of slab w is cluster rank w % S, slot (sender, kpart, w / S, m)
     const int owner = slab % S, lslab = slab / S;
     auto slot = [&](int sender, int m) {
       return recv + ((size_t(sender * KW + kpart) * nown_max + lslab) * MT + m) * kSlabCols + 4 * g;
     };
     if (S == 1) {
+      consumer_sync(nthr);  // the pieces overwrite the ring: every consumer is past its last stage
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int m = 2 * t + p;
-        if (m < MT)
-          *reinterpret_cast<float4*>(slot(0, m)) = make_float4(acc[0][p], acc[0][2 + p], acc[1][p], acc[1][2 + p]);
-      }
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const int m = 8 * nt + 2 * t + p;
+          if (m < MT)
+            *reinterpret_cast<float4*>(slot(0, m)) =
+                make_float4(acc[0][nt][p], acc[0][nt][2 + p], acc[1][nt][p], acc[1][nt][2 + p]);
+        }
       mbar_arrive(recv_bar);  // release: the stores above are visible to the waiter
     } else {
       __syncwarp();
       cluster_wait();
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int m = 2 * t + p;
-        if (m < MT)
-          st_async_v4_to_rank(smem_u32(slot(int(rank), m)), acc[0][p], acc[0][2 + p], acc[1][p], acc[1][2 + p],
-                              smem_u32(recv_bar), uint32_t(owner));
-      }
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const int m = 8 * nt + 2 * t + p;
+          if (m < MT)
+            st_async_v4_to_rank(smem_u32(slot(int(rank), m)), acc[0][nt][p], acc[0][nt][2 + p], acc[1][nt][p],
+                                acc[1][nt][2 + p], smem_u32(recv_bar), uint32_t(owner));
+        }
     }
   }
 
@@ -601,16 +630,17 @@ int groups_per_slice_max(int units, int S, int group) {
 // K-slices) are tried from the least work per CTA up; the first whose grid
 // runs in one wave (all T clusters resident at once -- on GB300 the SMs sit in
 // GPCs, so a cluster size that does not divide a GPC leaves SMs idle) is used.
-template <int ACT, bool HZ, bool PERM, bool TILED>
+template <int ACT, bool HZ, bool PERM, bool TILED, int NT>
 cudaError_t launch_4t(const Problem4T& pr) {
-  const void* kern = reinterpret_cast<const void*>(k4t_gemv_kernel<ACT, HZ, PERM, TILED>);
+  const void* kern = reinterpret_cast<const void*>(k4t_gemv_kernel<ACT, HZ, PERM, TILED, NT>);
   const int units = pr.K / kUnitK;
-  const int MT = pr.M <= 1 ? 1 : pr.M <= 2 ? 2 : pr.M <= 4 ? 4 : 8;
+  const int MT = NT > 1 ? 8 * NT : pr.M <= 1 ? 1 : pr.M <= 2 ? 2 : pr.M <= 4 ? 4 : 8;
+  const int max_slabs = PERM ? kMaxSlabsPerm : (NT == 4 ? 6 : 8);  // the kernel's thread bound
   const int max_smem = device_max_smem();
   struct Cand { long long cost; int S, nslab; };
   Cand cands[5 * 8];
   int nc = 0;
-  for (int nslab = 4; nslab <= (PERM ? kMaxSlabsPerm : 8); ++nslab)
+  for (int nslab = 4; nslab <= max_slabs; ++nslab)
     for (int S = 1; S <= 8 && S <= units; ++S)
       cands[nc++] = Cand{static_cast<long long>(nslab) * ((units + S - 1) / S), S, nslab};
   std::sort(cands, cands + nc, [](const Cand& a, const Cand& b) {
@@ -643,10 +673,10 @@ cudaError_t launch_4t(const Problem4T& pr) {
     const int ng = groups_per_slice_max(units, 1, pr.group);
     int NS = 3;
     const int kr = krange_max(units, 1);
-    size_t sm = Smem4T(8, NS, MT, 1, ng, PERM, kr).total;
-    while (sm > static_cast<size_t>(max_smem) && NS > 2) sm = Smem4T(8, --NS, MT, 1, ng, PERM, kr).total;
+    size_t sm = Smem4T(max_slabs, NS, MT, 1, ng, PERM, kr).total;
+    while (sm > static_cast<size_t>(max_smem) && NS > 2) sm = Smem4T(max_slabs, --NS, MT, 1, ng, PERM, kr).total;
     if (sm > static_cast<size_t>(max_smem)) return cudaErrorNotSupported;
-    q = Plan4T{8, 1, (pr.N + 255) / 256, NS, MT};
+    q = Plan4T{max_slabs, 1, (pr.N + max_slabs * kSlabCols - 1) / (max_slabs * kSlabCols), NS, MT};
     smem = sm;
     ng_max = ng;
   }
@@ -719,11 +749,20 @@ cudaError_t launch_wq4t(const void* x, const int32_t* qweight, const uint8_t* wt
                         int act_bf16, unsigned flags, cudaStream_t stream) {
   int gshift = 0;
   while ((kUnitK << gshift) < group) ++gshift;
-  if ((kUnitK << gshift) != group || K % kUnitK != 0 || M < 1 || M > 8) return cudaErrorNotSupported;
-  const Problem4T pr{x, qweight, wtiled, scales, qzeros, perm, y, M, K, N, group, gshift, flags, stream};
   const bool tiled = wtiled != nullptr, is_perm = perm != nullptr, hz = qzeros != nullptr;
+  // M <= 8: one n-tile; 9 .. 32 rows (GPTQ layout, contiguous groups): two or four
+  if ((kUnitK << gshift) != group || K % kUnitK != 0 || M < 1 || M > ((tiled || is_perm) ? 8 : 32))
+    return cudaErrorNotSupported;
+  const Problem4T pr{x, qweight, wtiled, scales, qzeros, perm, y, M, K, N, group, gshift, flags, stream};
 #define WQ4T_LAUNCH(ACT, HZ, PERM, TILED) \
-  if (act_bf16 == ACT && hz == HZ && is_perm == PERM && tiled == TILED) return launch_4t<ACT, HZ, PERM, TILED>(pr);
+  if (act_bf16 == ACT && hz == HZ && is_perm == PERM && tiled == TILED) return launch_4t<ACT, HZ, PERM, TILED, 1>(pr);
+#define WQ4T_LAUNCH_NT(ACT, HZ)                                                  \
+  if (act_bf16 == ACT && hz == HZ && !is_perm && !tiled)                         \
+    return M <= 16 ? launch_4t<ACT, HZ, false, false, 2>(pr) : launch_4t<ACT, HZ, false, false, 4>(pr);
+  if (M > 8) {
+    WQ4T_LAUNCH_NT(0, false) WQ4T_LAUNCH_NT(0, true) WQ4T_LAUNCH_NT(1, false) WQ4T_LAUNCH_NT(1, true)
+    return cudaErrorInvalidValue;
+  }
   WQ4T_LAUNCH(0, false, false, false) WQ4T_LAUNCH(0, false, false, true)
   WQ4T_LAUNCH(0, false, true, false) WQ4T_LAUNCH(0, false, true, true)
   WQ4T_LAUNCH(0, true, false, false) WQ4T_LAUNCH(0, true, false, true)
@@ -732,6 +771,7 @@ cudaError_t launch_wq4t(const void* x, const int32_t* qweight, const uint8_t* wt
   WQ4T_LAUNCH(1, false, true, false) WQ4T_LAUNCH(1, false, true, true)
   WQ4T_LAUNCH(1, true, false, false) WQ4T_LAUNCH(1, true, false, true)
   WQ4T_LAUNCH(1, true, true, false) WQ4T_LAUNCH(1, true, true, true)
+#undef WQ4T_LAUNCH_NT
 #undef WQ4T_LAUNCH
   return cudaErrorInvalidValue;
 }

@@ -303,14 +303,18 @@ def test_no_timeouts(G):
     assert wq.read_timeout_flag(clear=True) == 0
 
 
-# ------------------------------------------------------- tcgen05, M > 8 ----
+# ------------------------------------------------------------------ M > 8 ----
+# 9 .. 32 rows take the warp-level MMA kernel with two or four n-tiles (rows
+# past M inside an n-tile read TMA zero fill); more rows the tcgen05 kernel in
+# 64-row chunks, whose last chunk picks the 16-, 32- or 64-row instance
 WQ4_MMA_CASES = [  # M, K, N, group, bf16, asym zeros
     (16, 8192, 28672, 128, True, False), (32, 8192, 28672, 128, True, False),
     (16, 256, 128, 64, True, False), (17, 512, 264, 128, False, True), (33, 1024, 392, 256, True, True),
     (9, 2048, 1024, 128, False, False), (50, 1024, 520, 64, True, False), (100, 512, 256, 128, False, True),
     # one K slice per CTA with 16 / 32 scale groups and stored zeros: the scales and
     # zeros fetched eight groups ahead cross several chunks (128-k and 64-k stages)
-    (17, 2048, 20480, 128, False, True), (24, 2048, 20480, 64, True, True)]
+    (17, 2048, 20480, 128, False, True), (24, 2048, 20480, 64, True, True),
+    (80, 512, 264, 128, True, False), (96, 1024, 136, 64, False, True), (31, 4096, 1056, 128, True, True)]
 
 
 @pytest.mark.parametrize("M,K,N,g,bf16,asym", WQ4_MMA_CASES)
