@@ -533,7 +533,8 @@ def run_wq4_sweep(args, dev):
         nbytes = (K // 8) * N * 4 + (K // g) * N * 2 + M * K * 2 + M * N * 2
         gbs = nbytes / (ms * 1e-3) / 1e9
         lines.append({"workload": f"W4A16 sym g128 K={K} N={N} M={M}", "M": M,
-                      "path": "mma.sync m16n8k16 (warp-level tensor cores)" if M <= 8 else "tcgen05 (tensor memory)",
+                      "path": ("mma.sync m16n8k16 (warp-level tensor cores)"
+                               + ("" if M <= 8 else f", {2 if M <= 16 else 4} n-tiles of 8 rows")),
                       "us_per_call": ms * 1e3,
                       "achieved_GBps": gbs, "frac_of_hbm": gbs / peak, "peak_source": peak_kind,
                       "tflops": 2 * M * K * N / (ms * 1e-3) / 1e12})

@@ -167,6 +167,22 @@ __global__ void __launch_bounds__(256) w8a8_outlier_scan_kernel(const uint16_t* 
     if ((hit >> i) & 1u) flags[k + i] = 1;
 }
 
+// The outlier columns of X, transposed: xoT[j][m] = X[m, idx[j]] (raw bf16),
+// gathered once per call so that the GEMM epilogue of every column tile reads
+// each outlier column of its rows as one contiguous run instead of one
+// scattered 2-byte load per element and tile.  One thread per row m.
+__global__ void __launch_bounds__(256) w8a8_outlier_gather_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                  const int* __restrict__ idx,
+                                                                  const int* __restrict__ count,
+                                                                  uint16_t* __restrict__ xoT) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int m = blockIdx.x * 256 + threadIdx.x;
+  if (m >= M) return;
+  const int cnt = *count;
+  for (int j = 0; j < cnt; ++j) xoT[size_t(j) * M + m] = X[size_t(m) * K + idx[j]];
+}
+
 // The flagged columns in increasing order (idx) and their number (count, and
 // *count_out when given): one CTA, a block-wide exclusive scan of per-thread counts.
 __global__ void __launch_bounds__(1024) w8a8_outlier_compact_kernel(const int* __restrict__ flags, int K,
@@ -244,12 +260,13 @@ static_assert(kEpiCols == 64, "the epilogue loop reads 16-column groups of a 64-
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
 
 struct SmemW8A8 {
-  size_t x, w, sx, bars, misc, total;
+  size_t x, w, sx, pre, bars, misc, total;
   __host__ __device__ SmemW8A8() {
     size_t o = 0;
     x = o;    o += size_t(kNS) * kXBytes;     // also the output staging area at the end
     w = o;    o += size_t(kNSW) * kWBytes;
     sx = o;   o = align_up(o + kBM * 4, 16);
+    pre = o;  o = align_up(o + size_t(kOutChunk) * (kBM * 2 + kBN), 16);  // LLM.int8(): first outlier chunk
     bars = o; o = align_up(o + size_t(2 * kNS + 2 * kNSW + 4) * 8, 16);
     misc = o; o = align_up(o + 32, 16);
     total = o + 1024;
@@ -266,11 +283,12 @@ struct W8A8Args {
   const float* Sx;       // workspace copy written by the quantization kernel
   void* Y;
   int32_t* acc_out;
-  // LLM.int8() (all null otherwise): the outlier columns and their number, and
-  // the bf16 activations and int8 weights their 16-bit product reads
+  // LLM.int8() (all null otherwise): the outlier columns and their number, the
+  // gathered bf16 activations of those columns (xoT [count][M]) and the int8
+  // weights their 16-bit product reads
   const int* out_idx;
   const int* out_count;
-  const uint16_t* Xb;
+  const uint16_t* XoT;
   const int8_t* Wb;
   int M, K, N;
 };
@@ -459,6 +477,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cbase = half * kEpiCols;
     const float sw = (n0 + col < N) ? a.Sw[n0 + col] : 0.f;
     for (int r = et; r < kBM; r += kEpiThreads) sSx[r] = (m0 + r < M) ? a.Sx[m0 + r] : 0.f;
+    // LLM.int8(): the tile's share of the first kOutChunk outlier columns --
+    // activations (bf16, [j][m]) and weight rows (int8, [j][n]) -- fetched now,
+    // while the main loop runs: in the epilogue their three dependent global
+    // loads (count, column list, values) cost ~1-2 us per tile under load
+    uint16_t* pre_x = reinterpret_cast<uint16_t*>(smem + L.pre);
+    int8_t* pre_w = reinterpret_cast<int8_t*>(pre_x + kOutChunk * kBM);
+    const int cnt0 = OUTLIER ? min(kOutChunk, *a.out_count) : 0;
+    if (OUTLIER) {
+#pragma unroll 4
+      for (int t = 0; t < kOutChunk * kBM / kEpiThreads; ++t) {
+        const int i = et + t * kEpiThreads, j = i / kBM, m = i % kBM;  // j is the same across a warp
+        if (j < cnt0) pre_x[i] = (m0 + m < M) ? a.XoT[size_t(j) * M + m0 + m] : uint16_t(0);
+      }
+#pragma unroll 4
+      for (int t = 0; t < kOutChunk * kBN / kEpiThreads; ++t) {
+        const int i = et + t * kEpiThreads, j = i / kBN, n = i % kBN;
+        if (j < cnt0) pre_w[i] = (n0 + n < N) ? a.Wb[size_t(a.out_idx[j]) * N + n0 + n] : int8_t(0);
+      }
+    }
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cbase;
     uint32_t acc[kEpiCols];
 #pragma unroll
@@ -495,12 +532,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (OUTLIER) {
       // LLM.int8(): y += sum_j X[m, idx_j] * (Sw[n] * W[idx_j, n]) over the outlier
-      // columns, staged kOutChunk at a time in the (now free) X ring
+      // columns: the first kOutChunk prefetched, the rest staged kOutChunk at a
+      // time in the (now free) X ring
       const int cnt = *a.out_count;
       float* xo = reinterpret_cast<float*>(sX + kOutlierStage);  // [kBM][kOutChunk]
       float* wo = xo + kBM * kOutChunk;                           // [kOutChunk][kBN]
       int* sidx = reinterpret_cast<int*>(wo + kOutChunk * kBN);   // [kOutChunk] column indices
-      for (int j0 = 0; j0 < cnt; j0 += kOutChunk) {
+      asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // the prefetched chunk is complete
+      for (int j = 0; j < cnt0; ++j) {
+        const float sww = sw * static_cast<float>(pre_w[j * kBN + col]);
+#pragma unroll
+        for (int c = 0; c < kEpiCols; ++c)
+          acc[c] = __float_as_uint(fmaf(bf16_bits_to_f32(pre_x[j * kBM + cbase + c]), sww, __uint_as_float(acc[c])));
+      }
+      // further chunks (more than kOutChunk outlier columns): fetched here
+      for (int j0 = kOutChunk; j0 < cnt; j0 += kOutChunk) {
         const int nj = min(kOutChunk, cnt - j0);
         asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");  // the previous round is consumed
         if (et < kOutChunk) sidx[et] = et < nj ? a.out_idx[j0 + et] : 0;
@@ -511,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kBM * kOutChunk / kEpiThreads; ++t) {
           const int i = et + t * kEpiThreads;
           if (i < kBM * nj) {
-            const int m = i / nj, j = i % nj;
-            xo[m * kOutChunk + j] = (m0 + m < M) ? bf16_bits_to_f32(a.Xb[size_t(m0 + m) * K + sidx[j]]) : 0.f;
+            const int m = i % kBM, j = i / kBM;  // consecutive threads, consecutive rows of one column
+            xo[m * kOutChunk + j] = (m0 + m < M) ? bf16_bits_to_f32(a.XoT[size_t(j0 + j) * M + m0 + m]) : 0.f;
           }
         }
 #pragma unroll
@@ -577,11 +623,12 @@ size_t w8a8_workspace_bytes(int M, int K, int N) {
 }
 
 // LLM.int8() needs, after the plain workspace, the column flags and the list
-// of outlier columns (int [K] each) and their count.
+// of outlier columns (int [K] each), their count, and the gathered outlier
+// activations (bf16 [K][M] at most: every column could be an outlier).
 size_t w8a8_outlier_workspace_bytes(int M, int K, int N) {
   const size_t base = w8a8_workspace_bytes(M, K, N);
   if (base == 0) return 0;
-  return base + 2 * align_up(size_t(K) * 4, 256) + 256;
+  return base + 2 * align_up(size_t(K) * 4, 256) + 256 + align_up(size_t(K) * M * 2, 256);
 }
 
 cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y, int M, int K, int N,
@@ -598,6 +645,7 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
   int* oflags = nullptr;
   int* oidx = nullptr;
   int* ocount = nullptr;
+  uint16_t* xoT = nullptr;
   if (outlier_threshold) {
     uint8_t* o = static_cast<uint8_t*>(workspace) + w8a8_workspace_bytes(M, K, N);
     oflags = reinterpret_cast<int*>(o);
@@ -615,6 +663,11 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
     e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_compact_kernel), dim3(1), dim3(1024), 0,
                   flags | WQ_FLAG_PDL, stream, cargs);
     if (e != cudaSuccess) return e;
+    xoT = reinterpret_cast<uint16_t*>(o + 2 * align_up(size_t(K) * 4, 256) + 256);
+    void* gargs[] = {&Xp, &M, &K, &oidx, &ocount, &xoT};
+    e = launch_ex(reinterpret_cast<const void*>(w8a8_outlier_gather_kernel), dim3((M + 255) / 256), dim3(256), 0,
+                  flags | WQ_FLAG_PDL, stream, gargs);
+    if (e != cudaSuccess) return e;
   }
 
   // 1) per-row quantization
@@ -631,8 +684,7 @@ cudaError_t launch_w8a8(const void* X, const int8_t* W, const float* Sw, void* Y
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, N, K, N, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  W8A8Args args{Sw, sx, Y, acc_out, oidx, ocount, outlier_threshold ? Xp : nullptr, outlier_threshold ? W : nullptr,
-                M, K, N};
+  W8A8Args args{Sw, sx, Y, acc_out, oidx, ocount, xoT, outlier_threshold ? W : nullptr, M, K, N};
   const void* kern = outlier_threshold ? reinterpret_cast<const void*>(w8a8_mma_kernel<true>)
                                        : reinterpret_cast<const void*>(w8a8_mma_kernel<false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total));

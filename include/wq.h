@@ -317,7 +317,10 @@ WQ_API wq_status w8a8_gemm_outlier(const void* X, const int8_t* W, const float* 
                                    void* workspace, size_t workspace_bytes, unsigned flags,
                                    void* stream);
 
-/* Bytes of device workspace w8a8_gemm_outlier needs for this shape (0 on bad shape). */
+/* Bytes of device workspace w8a8_gemm_outlier needs for this shape (0 on bad
+ * shape): the workspace of w8a8_gemm, the column flags and the list of outlier
+ * columns (4 K bytes each), and room for the gathered bf16 activations of up
+ * to K outlier columns (2 K M bytes). */
 WQ_API size_t w8a8_gemm_outlier_workspace_bytes(int M, int K, int N);
 
 /* Bytes of device workspace w8a8_gemm needs for this shape (0 on bad shape). */
