@@ -93,14 +93,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (S > 1) cluster_wait();
   } else {
     const int tid = threadIdx.x;
+    // the CTA's scale rows: weight-side data, requested before the dependency
+    // wait but stored after it -- a store right after its load would hold the
+    // thread (and its wait) for the whole HBM latency; the first two float4 of
+    // each thread (all of them up to 16 groups) stay in registers meanwhile
     const float* SC = static_cast<const float*>(a.scales);
-    for (int i = tid; i < ng * (kBN / 4); i += kConsumerThreads) {
+    const int nsc = ng * (kBN / 4);
+    auto scale4 = [&](int i) {
       const int gr = i / (kBN / 4), c = 4 * (i % (kBN / 4));
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (n0 + c < N) v = *reinterpret_cast<const float4*>(SC + size_t(g0 + gr) * N + n0 + c);
-      reinterpret_cast<float4*>(scl)[i] = v;
-    }
+      if (i < nsc && n0 + c < N) v = *reinterpret_cast<const float4*>(SC + size_t(g0 + gr) * N + n0 + c);
+      return v;
+    };
+    const float4 s0 = scale4(tid), s1 = scale4(tid + kConsumerThreads);
     pdl_wait();
+    if (tid < nsc) reinterpret_cast<float4*>(scl)[tid] = s0;
+    if (tid + kConsumerThreads < nsc) reinterpret_cast<float4*>(scl)[tid + kConsumerThreads] = s1;
+    for (int i = tid + 2 * kConsumerThreads; i < nsc; i += kConsumerThreads) reinterpret_cast<float4*>(scl)[i] = scale4(i);
     consumer_sync(kConsumerThreads);  // the scale table is complete before any warp folds
 
     float2 acc[MT][2];
