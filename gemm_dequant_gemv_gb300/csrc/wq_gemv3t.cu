@@ -158,6 +158,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
+// Bytes global -> this CTA's shared memory by the TMA engine, completing on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 struct Args3T {
   const void* x;
   const int32_t* mat;
@@ -170,16 +178,17 @@ struct Args3T {
 };
 
 struct Smem3T {
-  size_t xg, xsu, recv, bar, flag, total;
+  size_t xraw, xg, xsu, recv, bar, flag, total;
   // row pitch of the pair-ordered x, in values: an odd multiple of 32 (64 bytes)
   __host__ __device__ static int xpitch(int kur) { return kur * kUnitK + 32; }
   __host__ __device__ Smem3T(int nslab, int M, int S, int kur) {
     const int KW = kWarps3 / nslab, nown = (nslab + S - 1) / S;
     size_t o = 0;
+    xraw = o;  o = align16(o + size_t(M) * kur * kUnitK * 2);  // x slice as stored (one bulk copy per row)
     xg = o;    o = align16(o + size_t(M) * xpitch(kur) * 2);
     xsu = o;   o = align16(o + size_t(M) * kur * 4);
     recv = o;  o = align16(o + size_t(S) * KW * nown * M * kSlabCols * 4);
-    bar = o;   o = align16(o + 8);
+    bar = o;   o = align16(o + 16);  // recv_bar, xbar
     flag = o;  o = align16(o + 16);
     total = o;
   }
@@ -214,6 +223,8 @@ __global__ void __maxnreg__(kMaxRegs3) k3t_gemv_kernel(const Args3T a) {
   float* xsu = reinterpret_cast<float*>(smem + L.xsu);
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+  uint64_t* xbar = recv_bar + 1;  // the x slice
+  const uint16_t* xraw = reinterpret_cast<const uint16_t*>(smem + L.xraw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -234,6 +245,7 @@ __global__ void __maxnreg__(kMaxRegs3) k3t_gemv_kernel(const Args3T a) {
   const int nmine = ub - ua;
 
   if (threadIdx.x == 0) {
+    mbar_init(xbar, 1);
     if (S == 1) {
       mbar_init(recv_bar, kThreads3);
     } else {
@@ -258,21 +270,32 @@ __global__ void __maxnreg__(kMaxRegs3) k3t_gemv_kernel(const Args3T a) {
   if (S > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
   pdl_wait();
+  // x of the CTA's K-slice as stored: one bulk copy per row (the TMA engine,
+  // not the warps' load queues, which still hold the weight loads issued
+  // before the wait: loads of x queued behind them took ~1 us)
+  const int k0 = u0 * kUnitK;
+  const int kcopy = max(0, min(nu * kUnitK, K - k0));  // values of the slice that exist (a multiple of 32)
+  if (threadIdx.x == 0 && kcopy > 0) {
+    mbar_expect_tx(xbar, uint32_t(M) * kcopy * 2);
+    for (int m = 0; m < M; ++m)
+      bulk_copy_g2s(smem + L.xraw + size_t(m) * a.kur * kUnitK * 2, static_cast<const uint16_t*>(a.x) + size_t(m) * K + k0,
+                    uint32_t(kcopy) * 2, xbar);
+  }
+  const bool x_ok = kcopy == 0 || __all_sync(0xffffffffu, mbar_wait(xbar, 0));
   {
     // x of this warp's units in pair order, xg[m][b * 32 + pos] (b: block within
     // the slice) with 16-byte chunk q of block b at q ^ (b % 4), and the sum of x
     // per unit.  Lane l takes 8 values (chunk c): block c / 4, codes 8 (l % 4) ..
     // +7; the 32 lanes cover two units.  Only this warp reads what it writes.
-    const uint16_t* X = static_cast<const uint16_t*>(a.x);
     const int q4 = lane & 3;
     const uint64_t prow = q4 == 0 ? kPosRow0 : q4 == 1 ? kPosRow1 : q4 == 2 ? kPosRow2 : kPosRow3;
     const int c_lo = (ua - u0) * (kUnitK / 8), c_hi = (ub - u0) * (kUnitK / 8);
-    const int k0 = u0 * kUnitK;
     for (int m = 0; m < M; ++m) {
       for (int c0 = c_lo; c0 < c_hi; c0 += 32) {  // warp-uniform trip count
-        const int c = c0 + lane, k = k0 + 8 * c;
+        const int c = c0 + lane;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < c_hi && k < K) v = *reinterpret_cast<const uint4*>(X + size_t(m) * K + k);  // K % 32 == 0
+        if (x_ok && c < c_hi && 8 * c < kcopy)
+          v = *reinterpret_cast<const uint4*>(xraw + size_t(m) * a.kur * kUnitK + 8 * c);
         const int b = c >> 2;
         uint16_t* dst = xg + size_t(m) * xp + size_t(b) * kBlockK;
         const uint32_t h[4] = {v.x, v.y, v.z, v.w};
@@ -405,6 +428,7 @@ __global__ void __maxnreg__(kMaxRegs3) k3t_gemv_kernel(const Args3T a) {
       if (e0 < total && j0 == 0 && n < N) Y[size_t(m) * N + n] = __float2half_rn(v);
     }
   }
+  if (!x_ok && threadIdx.x == 0) mbar_wait(xbar, 0);  // a copy still in flight lands before the CTA exits
 }
 
 }  // namespace
