@@ -37,19 +37,20 @@
 // unit a thread loads its block's three word rows of its four columns, three
 // 16-byte loads, and the eight lanes of one row read 128 contiguous bytes.
 // Each code is used by one MMA only, so staging the weights in shared memory
-// buys no reuse, and a TMA box with 128-byte rows streams at most ~32 GB/s per
-// SM on GB300 (measured).  The loads of a warp's first two units go out before
-// the dependency wait (weights do not depend on the previous kernel), later
-// ones two units ahead.
+// buys no reuse; a warp's share here is small (two units at 4096 x 4096), so
+// all of its loads are in flight before the dependency wait (weights do not
+// depend on the previous kernel), later ones two units ahead.
 //
 // A CTA is small -- 8 warps, at most 112 registers a thread, a few KB of
 // shared memory -- so that it fits on an SM beside the CTAs of the kernel
 // launched before it: with programmatic dependent launch it then starts, and
-// has its weights in registers, while that kernel is still running.  For the
-// same reason nothing after the dependency wait synchronises the CTA: each
-// warp stages the x of its own units in pair order (shared memory rows an odd
-// multiple of 64 bytes apart, 16-byte chunk q of block b at q ^ (b % 4): the
-// B loads are conflict-free) and adds up x per unit on the way (the zero term).
+// has its weights in registers, while that kernel is still running.  After
+// the wait, x of the CTA's K-slice arrives by one bulk copy per row (through
+// the TMA engine: per-thread loads of x queued behind the weight loads took
+// ~1 us), and each warp lays out the x of its own units in pair order
+// (shared memory rows an odd multiple of 64 bytes apart, 16-byte chunk q of
+// block b at q ^ (b % 4): the B loads are conflict-free), adding up x per unit
+// on the way (the zero term); no CTA-wide barrier follows.
 //
 // Work decomposition: a CTA owns nslab 32-column slabs and a K-slice of
 // 128-value units; each warp a contiguous run of units of one slab; the S CTAs
@@ -178,7 +179,7 @@ struct Args3T {
 };
 
 struct Smem3T {
-  size_t xraw, xg, xsu, recv, bar, flag, total;
+  size_t xraw, xg, xsu, recv, bar, total;
   // row pitch of the pair-ordered x, in values: an odd multiple of 32 (64 bytes)
   __host__ __device__ static int xpitch(int kur) { return kur * kUnitK + 32; }
   __host__ __device__ Smem3T(int nslab, int M, int S, int kur) {
@@ -189,7 +190,6 @@ struct Smem3T {
     xsu = o;   o = align16(o + size_t(M) * kur * 4);
     recv = o;  o = align16(o + size_t(S) * KW * nown * M * kSlabCols * 4);
     bar = o;   o = align16(o + 16);  // recv_bar, xbar
-    flag = o;  o = align16(o + 16);
     total = o;
   }
 };

@@ -1,4 +1,4 @@
-// wq_gemv4t.cu -- 4-bit weight-only GEMV / skinny GEMM (M <= 8) on the
+// wq_gemv4t.cu -- 4-bit weight-only GEMV / skinny GEMM (M <= 32) on the
 // warp-level tensor-core MMA (mma.sync m16n8k16, fp32 accumulate).
 //
 // Definition ("Quantization CUDA", Int4 Weight Only Quantization / Weight Store
@@ -11,8 +11,9 @@
 // fp32 FMA pipe, and packed fp32 FMAs contend with the logic pipe, so the
 // CUDA-core form (one PRMT and half a packed FMA per code) issues at well
 // under half of the SM's rate.  Here each code costs only its exact conversion
-// (5/8 of a logic op and 1/2 of a packed half op); the products of all M <= 8
-// rows of x come from one MMA per 256 codes:
+// (5/8 of a logic op and 1/2 of a packed half op); the products of up to 8
+// rows of x come from one MMA per 256 codes, and 9 - 32 rows from two or
+// four (n-tiles of 8 rows) that share the converted A fragments:
 //   * one LOP3 puts two nibbles into the mantissas of an fp16 (bf16) pair
 //     holding 1024 + q (128 + q), and one HSUB2 (or, for nibbles read in place
 //     at bit 4, one HFMA2 by 1/16) leaves q - z exactly: A is exact, and so are
@@ -32,9 +33,10 @@
 //   * GPTQ [K/8, N]: per stage and slab one 2D TMA box of 32 words x 64 word
 //     rows with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r%8));
 //     thread t's rows 2t, 2t+1 put the 8 lanes of every load phase on 8
-//     different chunks.  Boxes of 128-byte rows stream at most ~4.9 TB/s on
-//     GB300 from one issuing thread (measured), so the slabs' boxes are issued
-//     by one producer lane each.
+//     different chunks.  The slabs' boxes are issued by one producer lane
+//     each; the whole GPTQ matrix streams through such boxes at ~5.6 TB/s on
+//     GB300 when nothing is computed (measured), faster than per-thread
+//     16-byte loads or cp.async of the same words.
 //   * tiled (wq4_repack_tiled): the same words reordered once so that each
 //     1 KB block (one 64-value unit of one slab) is contiguous, each thread's
 //     16 bytes sit at lane * 16, and the blocks of one unit follow each other
@@ -46,7 +48,9 @@
 // through distributed shared memory.  nslab and S are chosen per shape so
 // that the whole grid is resident at once (about one CTA per SM).  Two
 // consumer warps per slab split each 512-value stage; the last warp is the
-// producer.  x is staged per stage by TMA next to the weights.
+// producer.  x is staged per stage by TMA next to the weights (all M rows;
+// with several n-tiles the rows past M are the box's zero fill).  Without a
+// cluster the partial sums reuse the weight ring once every consumer is done.
 // PERM (rows sorted by act-order group once ahead of time): sorted row i
 // multiplies x[perm[i]]; each CTA gathers x of its K-slice through perm into
 // shared memory once, right after the dependency wait.
