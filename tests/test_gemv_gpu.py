@@ -142,6 +142,43 @@ def test_wq3_onehot_exact(G):
         assert np.array_equal(y, oracle.round_f16(y_ref)), k
 
 
+def test_wq3_tensor_core_onehot_exact(G):
+    """The 3-bit tensor-core path (M >= 3) reads every code of a block through
+    its pair cover (16 pairs from seven 32-bit windows): one-hot rows of x at
+    all 32 positions of a block -- the straddling codes 10 and 21 included --
+    and at a few other blocks return the dequantized weight rows rounded once."""
+    import oracle
+    import synthetic as syn
+    d = syn.make_wq3(seed=7, M=8, K=512, N=264)
+    positions = list(range(32)) + [32 * 3 + 10, 32 * 6 + 21, 32 * 9 + 31, 32 * 15 + 0, 511, 300, 129, 64]
+    for c0 in range(0, len(positions), 8):
+        x = np.zeros((8, 512), np.float16)
+        for m, k in enumerate(positions[c0:c0 + 8]):
+            x[m, k] = 1.0
+        d["x"] = x
+        y = G.bits_u16(G.run_wq3(d))
+        y_ref, _ = oracle.wq3_gemv(x.view(np.uint16), d["mat"], d["scales"].view(np.uint16),
+                                   d["zeros"].view(np.uint16))
+        assert np.array_equal(y, oracle.round_f16(y_ref)), positions[c0:c0 + 8]
+
+
+def test_tensor_core_paths_repeat_bit_identical_and_pdl(G):
+    """The 3-bit tensor-core GEMM (M = 5) and the 4-bit n-tile GEMMs (M = 16,
+    24): two runs and a run with programmatic dependent launch give identical
+    bits (fixed summation order, no dependence on timing)."""
+    import gemm_dequant_gemv_gb300 as wq
+    import synthetic as syn
+    d3 = syn.make_wq3(seed=8, M=5, K=4096, N=4096)
+    a = G.bits_u16(G.run_wq3(d3))
+    assert np.array_equal(a, G.bits_u16(G.run_wq3(d3)))
+    assert np.array_equal(a, G.bits_u16(G.run_wq3(d3, flags=wq.WQ_FLAG_PDL)))
+    for M in (16, 24):
+        d4 = _make_wq4(M, 2048, 4096, 128, True, True, seed=9)
+        b = G.bits_u16(G.run_wq4(d4))
+        assert np.array_equal(b, G.bits_u16(G.run_wq4(d4)))
+        assert np.array_equal(b, G.bits_u16(G.run_wq4(d4, flags=wq.WQ_FLAG_PDL)))
+
+
 # ------------------------------------------------------------------- 4-bit ----
 WQ4_CASES = [  # M, K, N, group, bf16, asym zeros
     (1, 256, 128, 32, False, True), (3, 512, 264, 128, True, False), (8, 1024, 520, 64, False, True),
