@@ -61,6 +61,16 @@ def test_w8a8_parity_small(G, M, K, N):
     _check(G, d["X"], d["W"], d["Sw"])
 
 
+def test_w8a8_more_tiles_than_sms_ragged_odd_stages(G):
+    """187 output tiles (11 x 17, ragged in both M and N): more CTAs than SMs,
+    so later CTAs run on SMs whose previous CTA has just released its tensor
+    memory; K = 320 gives three 128-value stages (an odd count) and two exact
+    chunks, the second of one stage."""
+    import synthetic as syn
+    d = syn.make_w8a8(seed=11, M=1300, K=320, N=2064)
+    _check(G, d["X"], d["W"], d["Sw"])
+
+
 def test_w8a8_adversarial_full_magnitude(G):
     """Every code of X +-127 with aligned signs: |acc| up to K * 127 * 128 (133 M at
     K = 8192) with W = -128 in some columns, the edge of the exact 256-value chunk
